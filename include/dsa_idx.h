@@ -1,0 +1,225 @@
+/*
+ * dsa_idx.h — C ABI of the GB300 (sm_103a) DSA lightning-indexer library.
+ *
+ * The method (DeepSeek Sparse Attention "lightning indexer" forward):
+ *   per query token t and every causally visible key s of the same document
+ *     I[t,s] = sm_scale * sum_j w[t,j] * ReLU(q[t,j,:] . k[s,:])
+ *   over the indexer heads j (one key head shared by all query heads), then the
+ *   index_topk keys with the largest I are selected per query.
+ * Sources (the public Megatron-LM pull-request pages this library follows):
+ *   [P1] PR #8403 "cuDNN DSA indexer precision options": "What does this PR do?"
+ *        (dsa_indexer_rope_fp32, dsa_indexer_scoring_precision), "Motivation"
+ *        (BF16 materialised between key LayerNorm and RoPE), review finding 1
+ *        (_assert_supported_indexer_scoring(use_relu)), finding 2 (BF16 rounding
+ *        of FP32 carriers at the scoring boundary; worked example q=k=1.001),
+ *        finding 3 (_indexer_forward(q, k, w, ratio, sm_scale, precision) with
+ *        q (1,128,32,128) against k (1,128,1,128)).
+ *   [P2] PR #5992 "[DeepSeek-V4] Add compact BF16 and MXFP8 DSA indexer
+ *        support": "Key changes" (MXFP8 via BF16->MXFP8 quantisation, THD
+ *        cu_seqlens, caller-owned CUDA-graph-safe workspaces, deterministic
+ *        Top-K tie breaking), review "THD MXFP8 scale prefixes".
+ *   [P3] PR #7522 "KPool (pooled-key) DSA indexer support": "Changes"
+ *        (dsa_indexer_kpool, always_select_tail, THD restart, NoPE).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are caller-owned CUDA device pointers, 16-byte
+ *     aligned, row-major and contiguous.  The library never allocates, frees
+ *     or synchronises on them; every call is enqueued on the caller's stream
+ *     and returns as soon as the launches are queued (capturable in a CUDA
+ *     graph).  Sizes are passed by value so no device->host read is needed
+ *     ([P2] "Key changes": caller-owned workspaces, sizing done eagerly).
+ *   - Sequences are packed back to back (THD).  cu_seqlens is a device int32
+ *     array [num_seqs+1] with cu_seqlens[0]=0, non-decreasing, and
+ *     cu_seqlens[num_seqs]=total_tokens; queries and keys share it (T=S per
+ *     document, self attention).  A batch of equal-length sequences (BSHD) is
+ *     the special case of equal lengths.
+ *   - Causality: key s is visible to query t iff both lie in the same
+ *     document and s_local <= t_local (diagonal included).
+ *   - Indices written by the library are local to the document (0..len-1).
+ *   - Host-side argument errors return a code before anything is launched;
+ *     dsa_idx_last_error() gives the message.  Errors the device detects
+ *     (inconsistent cu_seqlens, a bounded wait that ran out) are recorded in
+ *     the status word at the head of the workspace; read them with
+ *     dsa_idx_read_status().
+ *   - MXFP8 tensors: payload bytes are OCP FP8 E4M3 codes, row-major like the
+ *     source; scales are UE8M0 bytes (value 2^(byte-127)), one per 32
+ *     consecutive elements along head_dim, stored row-major [rows, D/32].  The
+ *     scale layout does not depend on cu_seqlens (unlike the per-sequence
+ *     padded layout in [P2], whose prefixes can go stale under graph replay).
+ */
+#ifndef DSA_IDX_H_
+#define DSA_IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* dsa_stream_t;
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* bad pointer, size, or inconsistent cu_seqlens */
+  DSA_ERR_UNSUPPORTED = 2, /* shape / head count / device not supported */
+  DSA_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  DSA_ERR_WORKSPACE = 4,   /* workspace missing or too small */
+  DSA_ERR_TIMEOUT = 5      /* a device-side bounded wait gave up */
+} dsa_status_t;
+
+typedef enum { DSA_DTYPE_F32 = 0, DSA_DTYPE_BF16 = 1 } dsa_dtype_t;
+
+typedef enum { DSA_PREC_BF16 = 0, DSA_PREC_MXFP8 = 1 } dsa_precision_t;
+
+/* UE8M0 block-exponent rule of the MXFP8 quantiser.
+ * DSA_MX_SCALE_NOSAT (default): the smallest e with amax <= 448*2^e, so no
+ *   element saturates (the BF16->MXFP8 conversion of [P2] "Key changes").
+ * DSA_MX_SCALE_FLOOR: e = floor(log2(amax)) - 8, payload saturates at +-448. */
+typedef enum { DSA_MX_SCALE_NOSAT = 0, DSA_MX_SCALE_FLOOR = 1 } dsa_mx_scale_rule_t;
+
+/* dsa_idx_score_topk flags. */
+#define DSA_FLAG_DETERMINISTIC 0x1   /* [P2] deterministic Top-K tie break; always honoured */
+#define DSA_FLAG_SORT_BY_SCORE 0x2   /* rows in (score desc, index asc) order instead of index asc */
+#define DSA_FLAG_KPOOL_TAIL 0x4      /* [P3] always_select_tail: append the query's incomplete pool */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int dsa_idx_version(void);
+
+/* Message of the last host-side error in this thread ("" if none). */
+const char* dsa_idx_last_error(void);
+
+/* Human-readable name of a status code. */
+const char* dsa_idx_status_string(dsa_status_t s);
+
+/* Bytes of caller-owned device workspace dsa_idx_score_topk needs for these
+ * sizes (status word, device-built work list).  Pure host function.
+ * Returns 0 for invalid sizes. */
+size_t dsa_idx_workspace_size(int total_tokens, int num_seqs, int max_seqlen,
+                              int n_heads, int head_dim, int index_topk,
+                              int kpool_size, dsa_precision_t prec);
+
+/* Width (entries per query row) of the index / score outputs of
+ * dsa_idx_score_topk: index_topk, or index_topk + kpool_size - 1 in pool mode
+ * with DSA_FLAG_KPOOL_TAIL. */
+int dsa_idx_output_width(int index_topk, int kpool_size, int flags);
+
+/* Key LayerNorm -> RoPE -> quantise, fused ([P1] "What does this PR do?" and
+ * "Motivation": key LayerNorm then RoPE; rope_fp32 keeps the chain in FP32,
+ * otherwise BF16 is materialised after the LayerNorm and after RoPE; [P1]
+ * finding 2: BF16 scoring rounds FP32 carriers to BF16; [P2] "Key changes":
+ * MXFP8 scoring operands).  Queries get RoPE only.  [P3] "Changes": rope_dim=0
+ * is the NoPE indexer.
+ *   q       device [total_tokens, n_heads, head_dim], in_dtype
+ *   k       device [total_tokens, head_dim], in_dtype
+ *   ln_gamma, ln_beta  device fp32 [head_dim], or both NULL = no key LayerNorm
+ *   ln_eps  LayerNorm epsilon (biased variance)
+ *   rope_dim  rotary dims (first rope_dim of head_dim; 0 = NoPE; multiple of 8)
+ *   rope_base  theta_i = rope_base^(-2i/rope_dim); positions restart at 0 in
+ *             every document
+ *   rope_interleaved  0: rotate-half pairs (i, i+rope_dim/2); 1: pairs (2i, 2i+1)
+ *   out_prec BF16: q_out/k_out are bf16; MXFP8: e4m3 bytes + UE8M0 scales
+ *   q_out   device [total_tokens*n_heads, head_dim] (bf16 or u8)
+ *   q_scale_out device u8 [total_tokens*n_heads, head_dim/32] (MXFP8 only, else NULL)
+ *   k_out, k_scale_out  same for the keys ([total_tokens, ...])
+ * Supported: head_dim in {64,128} (MXFP8: 128), n_heads in {1..64}. */
+dsa_status_t dsa_idx_preprocess(
+    const void* q, const void* k, dsa_dtype_t in_dtype,
+    const float* ln_gamma, const float* ln_beta, float ln_eps,
+    const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+    int n_heads, int head_dim, int rope_dim, float rope_base,
+    int rope_interleaved, int rope_fp32, dsa_precision_t out_prec,
+    dsa_mx_scale_rule_t scale_rule,
+    void* q_out, uint8_t* q_scale_out, void* k_out, uint8_t* k_scale_out,
+    dsa_stream_t stream);
+
+/* Stand-alone BF16/FP32 -> MXFP8 quantisation ([P2] "Key changes": BF16 to
+ * MXFP8 with UE8M0 scales per 32 elements).
+ *   x        device [rows, cols] in_dtype
+ *   x_e4m3   device u8 [rows, cols]
+ *   x_ue8m0  device u8 [rows, cols/32]
+ * cols must be a multiple of 32 (64 or 128 for the scoring kernel). */
+dsa_status_t dsa_idx_quantize_mxfp8(const void* x, dsa_dtype_t in_dtype,
+                                    int64_t rows, int cols,
+                                    dsa_mx_scale_rule_t scale_rule,
+                                    uint8_t* x_e4m3, uint8_t* x_ue8m0,
+                                    dsa_stream_t stream);
+
+/* KPool key compression ([P3] "Changes", dsa_indexer_kpool > 1): in every
+ * document, each complete group of pool_size consecutive keys becomes
+ *   kbar_p = sum_i softmax_i(gate[p*P+i] + slot_bias[i]) * k[p*P+i]
+ * (softmax over the P slots, computed in FP32), stored as bf16.  Pooling
+ * restarts at document boundaries; an incomplete last group is not pooled.
+ *   k          device [total_tokens, head_dim] k_dtype
+ *   gate_bf16  device bf16 bits [total_tokens]
+ *   slot_bias  device fp32 [pool_size]
+ *   k_pooled   device bf16 [total_tokens / pool_size, head_dim]
+ *              (document d's pools are rows cu_pools[d] .. cu_pools[d+1]-1)
+ *   cu_pools   device int32 [num_seqs+1], written by this call
+ * Supported: pool_size in {2,4,8}, head_dim in {64,128}. */
+dsa_status_t dsa_idx_kpool_compress(
+    const void* k, dsa_dtype_t k_dtype, const uint16_t* gate_bf16,
+    const float* slot_bias, const int32_t* cu_seqlens, int num_seqs,
+    int total_tokens, int head_dim, int pool_size, uint16_t* k_pooled,
+    int32_t* cu_pools, dsa_stream_t stream);
+
+/* Fused score + top-k: q.k^T on tcgen05 tensor cores, ReLU, head-weighted
+ * sum, causal/document mask and a streaming per-query top-k that keeps the
+ * T x S score matrix on chip.  ([P1] findings 1-3, [P2] "Key changes",
+ * [P3] "Changes" for pool mode.)
+ *   q        device [total_tokens*n_heads, head_dim]: bf16 (BF16) or e4m3 (MXFP8)
+ *   q_scale  device u8 [total_tokens*n_heads, head_dim/32] (MXFP8), else NULL
+ *   k        device [total_tokens, head_dim]; in pool mode the pooled keys
+ *            [total_tokens/kpool_size, head_dim] from dsa_idx_kpool_compress
+ *   k_scale  device u8 [rows of k, head_dim/32] (MXFP8), else NULL
+ *   w        device [total_tokens, n_heads], w_dtype (FP32 or BF16)
+ *   sm_scale scalar multiplier of the score
+ *   index_topk  keys selected per query (pool mode: multiple of kpool_size;
+ *               kpool_size*... pools = index_topk / kpool_size)
+ *   prec     BF16 (kind::f16) or MXFP8 (block-scaled kind::mxf8f6f4)
+ *   flags    DSA_FLAG_* bits
+ *   kpool_size  1 = plain keys; >1 = pool mode (cu_pools required)
+ *   topk_idx    device int32 [total_tokens, W] (W = dsa_idx_output_width):
+ *               selected local indices, ascending (or by score with
+ *               DSA_FLAG_SORT_BY_SCORE), then -1 padding.  Pool mode: the
+ *               expanded tokens of the selected pools, then the tail tokens.
+ *   topk_score  device fp32 [total_tokens, W] or NULL: the score of each
+ *               entry (pooled score for pool tokens, +INF for tail tokens,
+ *               -INF for padding)
+ *   topk_len    device int32 [total_tokens] or NULL: valid entries per row
+ *   ws, ws_bytes  device workspace of dsa_idx_workspace_size() bytes
+ * Ties are broken towards the lower index; -0 and +0 compare equal.
+ * Supported: head_dim 128 (BF16 also 64), n_heads in {4,8,16,32,64},
+ * 1 <= index_topk <= 2048, max_seqlen <= 65536. */
+dsa_status_t dsa_idx_score_topk(
+    const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
+    const void* w, dsa_dtype_t w_dtype, float sm_scale,
+    const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+    int n_heads, int head_dim, int index_topk, dsa_precision_t prec, int flags,
+    int kpool_size, const int32_t* cu_pools,
+    int32_t* topk_idx, float* topk_score, int32_t* topk_len,
+    void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* Synchronise `stream` and return the device status word recorded in `ws` by
+ * the last dsa_idx_score_topk call on it (DSA_OK if none).  Eager helper; do
+ * not call it while capturing a graph. */
+dsa_status_t dsa_idx_read_status(const void* ws, dsa_stream_t stream,
+                                 dsa_status_t* out);
+
+/* Diagnostic: one tcgen05 tile of the scoring contraction, written raw.
+ * acc[r, c] = sum_d K[r, d] * Q[c, d] for r < 128 key rows starting at
+ * k_row0 and c < n_cols query rows starting at q_row0 (block-scaled for
+ * MXFP8), fp32 [128, n_cols] to `acc_out`.  Used by the tests to check the
+ * tensor-core operand layout in isolation; not on the hot path. */
+dsa_status_t dsa_idx_debug_mma_tile(
+    const void* q, const uint8_t* q_scale, int64_t q_rows, int64_t q_row0,
+    const void* k, const uint8_t* k_scale, int64_t k_rows, int64_t k_row0,
+    int head_dim, int n_cols, dsa_precision_t prec, float* acc_out,
+    void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_IDX_H_ */
