@@ -1,0 +1,376 @@
+"""Benchmark of the DSA lightning-indexer hot path on GB300.
+
+A step is one pass of the whole path over one batch: key LayerNorm -> RoPE ->
+MXFP8 quantisation (dsa_idx_preprocess) followed by the fused score + top-k
+(dsa_idx_score_topk), on the single-sequence workload T = S = 32768, 64
+indexer heads, head_dim 128 (64 RoPE + 64 NoPE), top-k 2048, MXFP8 scoring.
+Inputs are seeded synthetic data already resident in HBM; L2 is flushed
+between timed steps.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the
+same workload's query rows.  Under torchrun each rank runs its own replica
+of the workload (weak scaling); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_indexer_dsa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "fused indexer score+top-k queries/sec, TFLOP/s and % of GB300 BF16/FP8 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record():
+    """Per-launch DRAM bytes of the fused kernel from the committed ncu
+    summary, valid only while the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "score_topk_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for name in ("score_topk.cu", "dsa_device.cuh", "score_layout.h"):
+        with open(os.path.join(ROOT, "sparse_attention_indexer_dsa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec
+
+
+def oracle_sample_rate(wl, x, n_rows, seed=0):
+    """Queries/s of the CPU oracle on `n_rows` query rows of the workload
+    (uniformly spread positions), including the key-side preprocessing and
+    quantisation the rows need."""
+    import oracle.dsa_oracle as O
+    rng = np.random.default_rng(seed)
+    T = wl.total_tokens
+    rows = np.sort(rng.choice(T, size=n_rows, replace=False))
+    t0 = time.perf_counter()
+    cu = wl.cu_seqlens
+    pos = O.positions_in_document(cu)
+    kk = O.key_layernorm(x["k"], x["ln_gamma"], x["ln_beta"], 1e-6)
+    kk = O.round_fp32(O.apply_rope(kk, pos, wl.rope_dim, wl.rope_base))
+    kq = O.scoring_operand(kk, wl.prec)[0]
+    qrows = O.round_fp32(O.apply_rope(x["q"][rows].astype(np.float64), pos[rows][:, None], wl.rope_dim,
+                                      wl.rope_base))
+    qq = np.zeros((T, wl.n_heads, wl.head_dim))
+    qq[rows] = O.scoring_operand(qrows.reshape(-1, wl.head_dim), wl.prec)[0].reshape(len(rows), wl.n_heads, -1)
+    O.indexer_topk(qq, kq, x["w"].astype(np.float64), cu, wl.index_topk, rows=rows)
+    dt = time.perf_counter() - t0
+    return n_rows / dt, dt, rows
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    x = W.make_inputs(wl)
+    n_rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample_rate(wl, x, max(1, n_rows // 4), seed=99)
+    times, rates = [], []
+    for s in range(args.steps):
+        rate, dt, _ = oracle_sample_rate(wl, x, n_rows, seed=s)
+        times.append(dt)
+        rates.append(rate)
+    value = n_rows * args.steps / sum(times)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": "target: T=S=32768, 1 sequence, 64 heads, D=128 (64 RoPE + 64 NoPE), "
+                               "top-k 2048, MXFP8 scoring, key LayerNorm + RoPE in FP32",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_rows} query rows per step at seeded uniform positions, plus the "
+                                   "key-side LayerNorm/RoPE/quantisation those rows need"},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args, wl):
+    import torch
+    import sparse_attention_indexer_dsa_gb300 as dsa
+
+    world, rank, local = dist_setup(args.gpus)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    devn = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_kind = load_peaks()
+    x = W.make_inputs(wl, seed=wl.seed + rank)
+    T, H, D, K = wl.total_tokens, wl.n_heads, wl.head_dim, wl.index_topk
+    cu_np = wl.cu_seqlens
+    # resident inputs
+    q = torch.from_numpy(x["q"]).to(devn)
+    k = torch.from_numpy(x["k"]).to(devn)
+    w = torch.from_numpy(x["w"]).to(devn)
+    g = torch.from_numpy(x["ln_gamma"]).to(devn)
+    b = torch.from_numpy(x["ln_beta"]).to(devn)
+    cu = torch.from_numpy(cu_np).to(devn)
+    prec = wl.prec
+    ws = dsa.workspace(T, 1, wl.max_seqlen, H, D, K, 1, prec, devn)
+    q_op = torch.empty((T * H, D), dtype=torch.uint8, device=devn)
+    k_op = torch.empty((T, D), dtype=torch.uint8, device=devn)
+    q_sc = torch.empty((T * H, D // 32), dtype=torch.uint8, device=devn)
+    k_sc = torch.empty((T, D // 32), dtype=torch.uint8, device=devn)
+    idx = torch.empty((T, K), dtype=torch.int32, device=devn)
+    sco = torch.empty((T, K), dtype=torch.float32, device=devn)
+    lens = torch.empty((T,), dtype=torch.int32, device=devn)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=devn)
+    stream = torch.cuda.current_stream()
+
+    def pre():
+        dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False, True,
+                       prec, out=(q_op, q_sc, k_op, k_sc))
+
+    def score():
+        dsa.score_topk(q_op, q_sc, k_op, k_sc, w, cu, wl.max_seqlen, H, K, prec, ws=ws,
+                       out=(idx, sco, lens))
+
+    for _ in range(args.warmup):
+        pre()
+        score()
+    torch.cuda.synchronize()
+    st = dsa.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(devn.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)                      # L2 flush, outside the events
+        ev[s][0].record(stream)
+        pre()
+        ev[s][1].record(stream)
+        score()
+        ev[s][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    pre_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    sc_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    step_ms = [a + c for a, c in zip(pre_ms, sc_ms)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=devn)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st = dsa.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+
+    # end to end through the public API with host buffers (pinned), every step
+    hq = torch.from_numpy(x["q"]).pin_memory()
+    hk = torch.from_numpy(x["k"]).pin_memory()
+    hw = torch.from_numpy(x["w"]).pin_memory()
+    hidx = torch.empty((T, K), dtype=torch.int32).pin_memory()
+    hlen = torch.empty((T,), dtype=torch.int32).pin_memory()
+    h2d = hq.numel() * 4 + hk.numel() * 4 + hw.numel() * 4
+    d2h = hidx.numel() * 4 + hlen.numel() * 4
+    e2e_steps = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for s in range(e2e_steps):
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        pre()
+        score()
+        hidx.copy_(idx, non_blocking=True)
+        hlen.copy_(lens, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # optional BF16 scoring of the same workload (score kernel only)
+    bf16 = None
+    if not args.no_bf16:
+        qb = torch.empty((T * H, D), dtype=torch.bfloat16, device=devn)
+        kb = torch.empty((T, D), dtype=torch.bfloat16, device=devn)
+        dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False, True, "bf16",
+                       out=(qb, None, kb, None))
+        for _ in range(2):
+            dsa.score_topk(qb, None, kb, None, w, cu, wl.max_seqlen, H, K, "bf16", ws=ws, out=(idx, sco, lens))
+        bt = []
+        for s in range(3):
+            flush.fill_(s)
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            dsa.score_topk(qb, None, kb, None, w, cu, wl.max_seqlen, H, K, "bf16", ws=ws, out=(idx, sco, lens))
+            a1.record(stream)
+            torch.cuda.synchronize()
+            bt.append(a0.elapsed_time(a1))
+        bms = statistics.median(bt)
+        bf16 = {"score_ms": bms, "tflops": wl.flops() / bms / 1e9,
+                "frac_of_bf16_peak": wl.flops() / bms / 1e9 / peaks["bf16_tflops"],
+                "peak_tflops": peaks["bf16_tflops"], "peak_kind": peak_kind}
+
+    if rank != 0:
+        return
+    flops = wl.flops()
+    sc_avg = statistics.mean(sc_ms)
+    achieved = flops / sc_avg / 1e9                      # TFLOP/s
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    pre_bytes = T * H * D * 4 + T * D * 4 + T * H * D + T * H * D // 32 + T * D + T * D // 32
+    tr = traffic_record()
+    value = world * T * args.steps / (total_ms / 1e3)
+    cpu_rate, cpu_dt, _ = (None, None, None)
+    if not args.no_cpu:
+        cpu_rate, cpu_dt, _ = oracle_sample_rate(wl, x, args.ref_rows)
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (MXFP8) operands, fp32 accumulate",
+        "data": "synthetic (seeded PCG64), resident in HBM",
+        "config": {"workload": "target: T=S=32768, 1 sequence, 64 heads, D=128 (64 RoPE + 64 NoPE), "
+                               "top-k 2048, MXFP8 scoring, key LayerNorm + RoPE in FP32",
+                   "global_batch": world * T, "seq_len": T, "l2": "flushed (256 MB write) before every step",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": achieved, "frac_of_fp8_peak": achieved / fp8_peak,
+        "score_topk_ms": sc_avg, "preprocess_ms": statistics.mean(pre_ms),
+        "preprocess": {"bytes": pre_bytes, "GB/s": pre_bytes / statistics.mean(pre_ms) / 1e6,
+                       "frac_of_hbm": pre_bytes / statistics.mean(pre_ms) / 1e6 / peaks["hbm_gbs"]},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp8_peak,
+                     "peak_source": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} (nominal FP8/BF16)",
+                     "kernel": "score_topk (work-list build + fused kernel, events on the launch stream)",
+                     "traffic": tr["bytes_per_launch"] if tr else None},
+        "bf16_scoring": bf16,
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "queries/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pinned host q,k,w -> dsa_idx_preprocess -> dsa_idx_score_topk -> host top-k indices"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "wall_s": t_wall,
+        "cpu_baseline": None if cpu_rate is None else {
+            "value": cpu_rate, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{args.ref_rows} query rows of the target at seeded uniform positions "
+                      f"({cpu_dt:.1f} s), plus the key-side preprocessing they need"},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="target")
+    ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true")
+    args = ap.parse_args()
+    wl = W.config(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_native(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,48 @@
+// Kernel parameter blocks and launcher declarations shared by the C ABI
+// (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "score_layout.h"
+
+namespace dsa {
+
+struct PreParams {
+  const void* q;
+  const void* k;
+  const float* gamma;
+  const float* beta;
+  const int32_t* cu;
+  void* q_out;
+  uint8_t* q_scale;
+  void* k_out;
+  uint8_t* k_scale;
+  double inv_freq[64];
+  float eps;
+  int in_bf16, num_seqs, total_tokens, H, rope_dim, interleaved, rope_fp32, out_mx, scale_rule;
+};
+
+struct DebugParams {
+  CUtensorMap tm_q, tm_k, tm_qs, tm_ks;
+  int64_t q_row0, k_row0;
+  int chunks, n_cols;
+  float* out;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_preprocess(const PreParams& p, int D, cudaStream_t stream);
+cudaError_t launch_quantize_mxfp8(const void* x, int in_bf16, int64_t nblocks, int rule,
+                                  uint8_t* out, uint8_t* scales, int sm_count, cudaStream_t stream);
+cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const float* bias,
+                         const int32_t* cu, int num_seqs, int total_tokens, int D, int P,
+                         uint16_t* out, int32_t* cu_pools, int sm_count, cudaStream_t stream);
+cudaError_t launch_build_worklist(const int32_t* cu, int num_seqs, int total_tokens, int max_seqlen,
+                                  int tq, int pool, int2* items, int* doc_prefix, int* hdr,
+                                  int max_items, cudaStream_t stream);
+cudaError_t launch_score_topk(const ScoreParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_debug_mma_tile(const DebugParams& p, int prec, cudaStream_t stream);
+
+}  // namespace dsa

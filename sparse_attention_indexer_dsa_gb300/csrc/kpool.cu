@@ -1,0 +1,119 @@
+// KPool key compression for sm_103a (Megatron-LM PR #7522 "KPool (pooled-key)
+// DSA indexer support", "Changes"): in each document, every complete group of
+// P consecutive keys becomes sum_i softmax_i(gate_i + bias_i) * k_i (softmax
+// over the P slots in FP32, BF16 gate, FP32 per-slot bias), stored as BF16.
+// Pooling restarts at document boundaries; a trailing incomplete group is not
+// pooled.  HBM-bound: one warp per pool, 128-bit loads.
+#include <cuda_bf16.h>
+
+#include "dsa_device.cuh"
+#include "dsa_params.h"
+
+namespace dsa {
+
+// cu_pools[d] = sum over earlier documents of floor(L / P); one block.
+__global__ void __launch_bounds__(1024) kpool_cu_kernel(const int32_t* __restrict__ cu, int num_seqs,
+                                                       int P, int32_t* __restrict__ cu_pools) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x;
+  int carry = 0;
+  for (int base = 0; base < num_seqs; base += 1024) {
+    const int d = base + tid;
+    const int v = d < num_seqs ? (cu[d + 1] - cu[d]) / P : 0;
+    int x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((tid & 31) >= o) x += y;
+    }
+    if ((tid & 31) == 31) warp_tot[tid >> 5] = x;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < (tid >> 5); ++w) before += warp_tot[w];
+    if (d < num_seqs) cu_pools[d] = carry + before + x - v;
+    int tot = 0;
+    for (int w = 0; w < 32; ++w) tot += warp_tot[w];
+    __syncthreads();
+    carry += tot;
+  }
+  if (tid == 0) cu_pools[num_seqs] = carry;
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(256) kpool_compress_kernel(
+    const void* __restrict__ k, int k_bf16, const uint16_t* __restrict__ gate,
+    const float* __restrict__ bias, const int32_t* __restrict__ cu,
+    const int32_t* __restrict__ cu_pools, int num_seqs, int max_pools, int P,
+    uint16_t* __restrict__ out) {
+  constexpr int D = VEC * 32;
+  const int lane = threadIdx.x & 31;
+  const int total = cu_pools[num_seqs];
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int pi = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pi < total && pi < max_pools;
+       pi += nwarps) {
+    int lo = 0, hi = num_seqs - 1;   // document of pool pi
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu_pools[mid] <= pi) lo = mid; else hi = mid - 1;
+    }
+    const int tok0 = cu[lo] + (pi - cu_pools[lo]) * P;
+    float logit[8];
+    float mx = -INFINITY;
+    for (int i = 0; i < P; ++i) {
+      logit[i] = __uint_as_float((uint32_t)__ldg(gate + tok0 + i) << 16) + __ldg(bias + i);
+      mx = fmaxf(mx, logit[i]);
+    }
+    float den = 0.f;
+    for (int i = 0; i < P; ++i) {
+      logit[i] = expf(logit[i] - mx);
+      den += logit[i];
+    }
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+    for (int i = 0; i < P; ++i) {
+      const float wgt = logit[i] / den;
+      const size_t row = (size_t)(tok0 + i) * D + lane * VEC;
+      float x[VEC];
+      if (k_bf16) {
+        const uint16_t* kp = reinterpret_cast<const uint16_t*>(k) + row;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[e] = __uint_as_float((uint32_t)__ldg(kp + e) << 16);
+      } else {
+        const float* kp = reinterpret_cast<const float*>(k) + row;
+        if constexpr (VEC == 4) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(kp));
+          x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+        } else {
+          const float2 f = __ldg(reinterpret_cast<const float2*>(kp));
+          x[0] = f.x; x[1] = f.y;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(wgt, x[e], acc[e]);
+    }
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)pi * D + lane * VEC;
+#pragma unroll
+    for (int e = 0; e < VEC; e += 2) *reinterpret_cast<__nv_bfloat162*>(o + e) = __floats2bfloat162_rn(acc[e], acc[e + 1]);
+  }
+}
+
+cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const float* bias,
+                         const int32_t* cu, int num_seqs, int total_tokens, int D, int P,
+                         uint16_t* out, int32_t* cu_pools, int sm_count, cudaStream_t stream) {
+  kpool_cu_kernel<<<1, 1024, 0, stream>>>(cu, num_seqs, P, cu_pools);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int max_pools = total_tokens / P;
+  if (max_pools == 0) return cudaSuccess;
+  int blocks = (max_pools + 7) / 8;
+  if (blocks > sm_count * 8) blocks = sm_count * 8;
+  if (D == 128)
+    kpool_compress_kernel<4><<<blocks, 256, 0, stream>>>(k, k_bf16, gate, bias, cu, cu_pools, num_seqs,
+                                                        max_pools, P, out);
+  else
+    kpool_compress_kernel<2><<<blocks, 256, 0, stream>>>(k, k_bf16, gate, bias, cu, cu_pools, num_seqs,
+                                                        max_pools, P, out);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
