@@ -37,6 +37,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 
 
+def describe(wl):
+    return (f"{wl.name}: {len(wl.doc_lens)} x {wl.max_seqlen} tokens (T={wl.total_tokens}), {wl.n_heads} heads, "
+            f"D={wl.head_dim} ({wl.rope_dim} RoPE + {wl.head_dim - wl.rope_dim} NoPE), top-k {wl.index_topk}, "
+            f"{wl.prec.upper()} scoring" + (", key LayerNorm + RoPE in FP32" if wl.layernorm else ""))
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -169,9 +175,7 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded PCG64)",
-        "config": {"workload": "target: T=S=32768, 1 sequence, 64 heads, D=128 (64 RoPE + 64 NoPE), "
-                               "top-k 2048, MXFP8 scoring, key LayerNorm + RoPE in FP32",
-                   "l2": "n/a (CPU)"},
+        "config": {"workload": describe(wl), "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n_rows} query rows per step at seeded uniform positions, plus the "
                                    "key-side LayerNorm/RoPE/quantisation those rows need"},
@@ -204,7 +208,7 @@ def run_native(args, wl):
     b = torch.from_numpy(x["ln_beta"]).to(devn)
     cu = torch.from_numpy(cu_np).to(devn)
     prec = wl.prec
-    ws = dsa.workspace(T, 1, wl.max_seqlen, H, D, K, 1, prec, devn)
+    ws = dsa.workspace(T, len(wl.doc_lens), wl.max_seqlen, H, D, K, 1, prec, devn)
     q_op = torch.empty((T * H, D), dtype=torch.uint8, device=devn)
     k_op = torch.empty((T, D), dtype=torch.uint8, device=devn)
     q_sc = torch.empty((T * H, D // 32), dtype=torch.uint8, device=devn)
@@ -326,8 +330,7 @@ def run_native(args, wl):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (MXFP8) operands, fp32 accumulate",
         "data": "synthetic (seeded PCG64), resident in HBM",
-        "config": {"workload": "target: T=S=32768, 1 sequence, 64 heads, D=128 (64 RoPE + 64 NoPE), "
-                               "top-k 2048, MXFP8 scoring, key LayerNorm + RoPE in FP32",
+        "config": {"workload": describe(wl),
                    "global_batch": world * T, "seq_len": T, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "tflops": achieved, "frac_of_fp8_peak": achieved / fp8_peak,
