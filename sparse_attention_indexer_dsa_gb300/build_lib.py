@@ -43,18 +43,22 @@ def _headers():
     return hs
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile and link; returns the library path."""
+def build(verbose: bool = False, force: bool = False, defines=(), build_dir: str = BUILD,
+          lib_path: str = LIB) -> str:
+    """Compile and link; returns the library path.  `defines` (e.g.
+    DSA_PHASE_TIMERS) go to every translation unit; use a separate build_dir
+    and lib_path for such variants."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "host_arch")
+    BUILD_, LIB_ = build_dir, lib_path
+    os.makedirs(BUILD_, exist_ok=True)
+    stamp = os.path.join(BUILD_, "host_arch")
     arch = platform.machine()
     if not os.path.exists(stamp) or open(stamp).read().strip() != arch:
         force = True          # objects from another host architecture are never reused
     newest_header = max(os.path.getmtime(h) for h in _headers())
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_, os.path.basename(src)[:-3] + ".o")
         stale = force or not os.path.exists(obj) or os.path.getmtime(obj) < max(
             os.path.getmtime(src), newest_header)
         if stale:
@@ -62,7 +66,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     def compile_one(job):
         src, obj = job
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj + ".tmp"]
+        cmd = [nvcc, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c", src, "-o", obj + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -73,18 +77,18 @@ def build(verbose: bool = False, force: bool = False) -> str:
     if jobs:
         with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
             list(ex.map(compile_one, jobs))
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in _sources()]
-    if jobs or force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(map(os.path.getmtime, objs)):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-Xcompiler", "-fPIC"]
+    objs = [os.path.join(BUILD_, os.path.basename(s)[:-3] + ".o") for s in _sources()]
+    if jobs or force or not os.path.exists(LIB_) or os.path.getmtime(LIB_) < max(map(os.path.getmtime, objs)):
+        cmd = [nvcc, *ARCH, "-shared", "-o", LIB_ + ".tmp", *objs, "-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB + ".tmp", LIB)
+        os.replace(LIB_ + ".tmp", LIB_)
         if verbose:
-            print(f"linked {LIB}", flush=True)
+            print(f"linked {LIB_}", flush=True)
     with open(stamp, "w") as f:
         f.write(arch)
-    return LIB
+    return LIB_
 
 
 if __name__ == "__main__":

@@ -12,7 +12,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/dsa_idx.h"
+#include "dsa_idx.h"
 #include "dsa_status_codes.h"
 #include "dsa_params.h"
 
@@ -81,14 +81,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Operand [rows, D] (bf16 or u8), box 128 rows x 128 bytes, 128-byte swizzle.
-dsa_status_t make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int D, bool fp8) {
+// Operand [rows, D] (bf16 or u8), box box_rows x 128 bytes, 128-byte swizzle.
+dsa_status_t make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int D, bool fp8,
+                              int box_rows = kTileKeys) {
   auto enc = encode_fn();
   if (!enc) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   const int elem = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)D * elem};
-  cuuint32_t box[2] = {(cuuint32_t)(kChunkBytes / elem), (cuuint32_t)kTileKeys};
+  cuuint32_t box[2] = {(cuuint32_t)(kChunkBytes / elem), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -298,7 +299,8 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   if (s != DSA_OK) return s;
   const bool fp8 = pl_prec == PREC_MXFP8;
   const int64_t krows = kpool_size > 1 ? total_tokens / kpool_size : total_tokens;
-  if ((s = make_operand_map(&p.tm_q, q, (int64_t)total_tokens * n_heads, head_dim, fp8)) != DSA_OK) return s;
+  if ((s = make_operand_map(&p.tm_q, q, (int64_t)total_tokens * n_heads, head_dim, fp8, p.plan.nsub)) != DSA_OK)
+    return s;
   if ((s = make_operand_map(&p.tm_k, k, krows, head_dim, fp8)) != DSA_OK) return s;
   if (fp8) {
     if ((s = make_scale_map(&p.tm_qs, q_scale, (int64_t)total_tokens * n_heads)) != DSA_OK) return s;

@@ -67,6 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is
+// still pending (it resumes as soon as the phase completes), so waiting warps
+// do not spin and take issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kWaitHintNs = 20000;
+
 // Bounded wait on phase `parity`.  Gives up after timeout_ns (or as soon as
 // another thread of the CTA has raised *abort), records DSA_ERR_TIMEOUT in the
 // status word and returns false.  Never traps and never spins forever.
@@ -74,15 +91,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           int* status, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) {
-        set_status(status, DSA_DEV_ERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      set_status(status, DSA_DEV_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
     }
   }
 }
@@ -236,6 +251,25 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
+// tcgen05.wait::ld that also names the destination registers of the loads it
+// waits for, so the compiler cannot move their uses above the wait.
+template <int N>
+__device__ __forceinline__ void tmem_wait_tied(uint32_t* r) {
+  static_assert(N == 4 || N == 8 || N == 16, "tied wait covers 4, 8 or 16 registers");
+  if constexpr (N == 4) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3])::"memory");
+  } else if constexpr (N == 8) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7])::"memory");
+  } else {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
+  }
+}
+
 // ----------------------------------------------------------------------------
 // UMMA descriptors
 // ----------------------------------------------------------------------------
@@ -309,12 +343,7 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ra, rb, rc, rd;
-  ra = (uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32);
-  rb = (uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32);
-  rc = (uint64_t)__float_as_uint(c.x) | ((uint64_t)__float_as_uint(c.y) << 32);
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  return make_float2(__uint_as_float((uint32_t)rd), __uint_as_float((uint32_t)(rd >> 32)));
+  return __ffma2_rn(a, b, c);   // packed fma.rn.f32x2 (sm_100+), operands in register pairs
 }
 
 }  // namespace dsa

@@ -9,9 +9,10 @@ namespace dsa {
 
 enum { PREC_BF16 = 0, PREC_MXFP8 = 1 };
 
-constexpr int kScoreThreads = 320;   // warp 0: TMA, warp 1: MMA + TMEM, warps 2..9: epilogue
+constexpr int kEpiWGs = 4;           // epilogue warpgroups
+constexpr int kScoreThreads = 64 + 128 * kEpiWGs;   // warp 0: TMA, warp 1: MMA + TMEM, then epilogue
 constexpr int kEpiWarp0 = 2;
-constexpr int kG = 2;                // query sub-blocks (= epilogue warpgroups) per work item
+constexpr int kG = 2;                // query sub-blocks (UMMA B operands) per work item
 constexpr int kTileKeys = 128;       // keys per tcgen05 tile (UMMA M)
 constexpr int kChunkBytes = 128;     // bytes of one K-major row per smem chunk (128B swizzle)
 constexpr int kStageBytes = kTileKeys * kChunkBytes;   // 16 KiB
@@ -19,7 +20,10 @@ constexpr int kSfRawWords = 132;     // 128 scale words + up to 3 words of misal
 constexpr int kSfRawBytes = 640;     // kSfRawWords*4 = 528, padded to a 128-byte multiple
 constexpr int kSfTxBytes = 512;      // 32 rows x 16 bytes: the tcgen05.cp source layout
 constexpr int kMaxSmem = 232448;     // 227 KiB opt-in per block on sm_100/sm_103
-constexpr int kMiscInts = 128;       // per-warpgroup scratch ints
+constexpr int kMiscInts = 320;       // per-warpgroup scratch ints
+constexpr int kBatch = 4;            // key tiles scored between two appends
+constexpr int kMaxQpw = 4;           // queries per epilogue warpgroup (at most)
+constexpr int kEpiBarAll = 1 + kEpiWGs;   // named barrier of all epilogue warps (1..kEpiWGs: per warpgroup)
 constexpr int kMaxStages = 6;
 constexpr int kMaxQs = 8;
 constexpr int kMaxCand = 4096;
@@ -34,6 +38,7 @@ struct ScorePlan {
   int nst;       // K-tile smem stages
   int chunks;    // 128-byte chunks per operand row: head_dim*elem/128
   int tslots;    // TMEM accumulator slots of 128 columns
+  int qchunk;    // bytes of one q-operand chunk: nsub rows x 128 bytes (TMA box of the q map)
   // byte offsets into dynamic shared memory (base 1024-aligned)
   int q_off, k_off, sfa_raw_off, sfa_tx_off, sfb_raw_off, sfb_tx_off;
   int cand_key_off, cand_idx_off, w_off, hist_off, misc_off, bar_off, total;
@@ -76,24 +81,26 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
   s.tslots = prec == PREC_BF16 ? 4 : 3;
   int qs = 128 / n_heads;
   if (qs > kMaxQs) qs = kMaxQs;
-  int cand = round_up(keep * 2 > keep + 128 ? keep * 2 : keep + 128, 128);
-  if (cand > kMaxCand) cand = round_up(keep + 128, 128);
+  const int cand_min = keep + (kBatch + 2) * kTileKeys;   // a full batch fits after a shrink
+  int cand = round_up(keep * 2 > cand_min ? keep * 2 : cand_min, 128);
+  if (cand > kMaxCand) cand = round_up(cand_min, 128);
   if (cand > kMaxCand) return false;
   for (;;) {
-    if (qs * n_heads < 16) return false;
+    if (qs * n_heads < 16 || (qs * kG) % kEpiWGs != 0) return false;
     s.qs = qs;
     s.nsub = qs * n_heads;
     s.cand = cand;
+    s.qchunk = s.nsub * kChunkBytes;   // a multiple of 1024 (nsub % 16 == 0): keeps the swizzle atoms aligned
     // fixed part
     int off = 0;
     s.q_off = off;
-    off += kG * s.chunks * kStageBytes;
+    off += kG * s.chunks * s.qchunk;
     s.k_off = off;
     // the rest, independent of the stage count
     int rest = 0;
     const int sf = prec == PREC_MXFP8;
     int cand_bytes = kG * qs * cand * 6;
-    rest += cand_bytes + kG * qs * n_heads * 4 + kG * 256 * 4 + kG * kMiscInts * 4 + 512;
+    rest += cand_bytes + kG * qs * n_heads * 4 + kEpiWGs * 256 * 4 + kEpiWGs * kMiscInts * 4 + 512;
     int per_stage = kStageBytes + (sf ? kSfRawBytes + kSfTxBytes : 0);
     int sfb = sf ? kG * (kSfRawBytes + kSfTxBytes) : 0;
     int nst = (kMaxSmem - 1024 - off - rest - sfb) / per_stage;
@@ -117,9 +124,9 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
       s.w_off = off;
       off += kG * qs * n_heads * 4;
       s.hist_off = off;
-      off += kG * 256 * 4;
+      off += kEpiWGs * 256 * 4;
       s.misc_off = off;
-      off += kG * kMiscInts * 4;
+      off += kEpiWGs * kMiscInts * 4;
       off = round_up(off, 8);
       s.bar_off = off;
       off += 512;
@@ -127,14 +134,14 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
       *p = s;
       return s.total <= kMaxSmem;
     }
-    if (cand > round_up(keep + 128, 128)) {
-      cand = round_up(keep + 128, 128);
+    if (cand > round_up(cand_min, 128)) {
+      cand = round_up(cand_min, 128);
       continue;
     }
-    if (qs > 1 && (qs / 2) * n_heads >= 16) {
+    if (qs > 2 && (qs / 2) * n_heads >= 16) {   // qs stays even: kG*qs splits over kEpiWGs
       qs /= 2;
-      cand = round_up(keep * 2 > keep + 128 ? keep * 2 : keep + 128, 128);
-      if (cand > kMaxCand) cand = round_up(keep + 128, 128);
+      cand = round_up(keep * 2 > cand_min ? keep * 2 : cand_min, 128);
+      if (cand > kMaxCand) cand = round_up(cand_min, 128);
       continue;
     }
     return false;

@@ -32,6 +32,22 @@
 
 namespace dsa {
 
+// Optional per-phase cycle counters (compile with -DDSA_PHASE_TIMERS; off in
+// the product build).  Each role accumulates clock64() deltas in registers
+// and adds them to g_phase_cycles once, at exit.
+#ifdef DSA_PHASE_TIMERS
+__device__ unsigned long long g_phase_cycles[64];
+#define PT_DECL unsigned long long pt_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}; long long pt_t0 = clock64();
+#define PT_MARK() (pt_t0 = clock64())
+#define PT_ADD(i) do { const long long pt_t1 = clock64(); pt_acc[i] += (unsigned long long)(pt_t1 - pt_t0); pt_t0 = pt_t1; } while (0)
+#define PT_FLUSH(base, rec) do { if (rec) for (int i_ = 0; i_ < 8; ++i_) atomicAdd(&g_phase_cycles[(base) + i_], pt_acc[i_]); } while (0)
+#else
+#define PT_DECL
+#define PT_MARK() ((void)0)
+#define PT_ADD(i) ((void)0)
+#define PT_FLUSH(base, rec) ((void)0)
+#endif
+
 // ----------------------------------------------------------------------------
 // Work list: items (document, first query) sorted by descending tile count so
 // the persistent CTAs take the longest items first.  One block.
@@ -166,7 +182,7 @@ __device__ __forceinline__ Item load_item(const ScoreParams& p, int i) {
 // Bounded wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitHintNs)) {
     if (globaltimer_ns() - t0 > timeout_ns) return;
   }
 }
@@ -200,44 +216,70 @@ __device__ __forceinline__ int warp_incl_scan(int x, uint32_t lane) {
 
 // misc scratch (ints) per epilogue warpgroup
 enum {
-  MS_WCNT = 0,          // [2][kMaxQs][4] append counts
-  MS_WTOT = 64,         // [4] scan warp totals
-  MS_DIGIT = 68,
-  MS_ABOVE = 69,
-  MS_BIN = 70,
-  MS_GT = 72,           // [4]
-  MS_EQ = 76,           // [4]
+  MS_WTOT = 0,          // [4] scan warp totals
+  MS_DIGIT = 4,
+  MS_ABOVE = 5,
+  MS_BIN = 6,
+  MS_GT = 8,            // [4]
+  MS_EQ = 12,           // [4]
+  MS_MIN = 16,          // [4]
+  MS_MAX = 20,          // [4]
+  MS_RCNT = 24,         // [2][8] per-warp counts of a compaction round
+  MS_BCNT = 48,         // [2][kBatch][kMaxQpw][4] per-warp append counts of a batch
+  MS_CAND = 176,
+  MS_CNT4 = 180,        // [4]
+  MS_SORT = 192,        // [128] sample keys (sort exchange)
 };
 
-// Keep exactly `keep` of the n (> keep) candidates of one query: the largest
-// keys, ties to the earlier buffer position (= lower index, the buffer is in
-// index order).  Stable in place.  Returns a threshold key: every future
-// candidate must be strictly larger.  All 128 threads of the warpgroup.
-template <int MMAX>
-__device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n, int keep, int wq,
-                              uint32_t lane, int* hist, int* ms, int bar_id) {
+// Shrink the n candidates of one query (n > keep).  The buffer holds
+// orderable score keys in index order.  Radix select on key - kmin, 8-bit
+// digits from the highest bit in which the buffer's keys differ:
+//  * exact: keeps exactly `keep` entries, the largest keys with ties to the
+//    earlier position (= lower index); returns the keep-th key, so a later
+//    candidate must be strictly larger.
+//  * approximate (exact == false): stops at the first digit level where
+//    keeping the whole boundary bin leaves at most cap_after entries; keeps
+//    every entry in or above that bin (never fewer than `keep`) and returns
+//    the bin's lower edge minus one, a threshold no larger than the true
+//    keep-th key, so no member of the final top-k is ever rejected.
+// Histogram passes re-read the keys from shared memory; the stable in-place
+// compaction runs in rounds of 512 entries (writes of a round land below the
+// next round's inputs).  *count_out receives the number kept.  All 128
+// threads of the warpgroup.
+__device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n, int keep,
+                                           bool exact, int cap_after, int wq, uint32_t lane,
+                                           int* hist, int* ms, int bar_id, int* count_out) {
   const int tid = wq * 32 + (int)lane;
-  const int span = ((n + 127) >> 7) << 5;    // entries per warp, multiple of 32
-  const int base = wq * span;
-  uint32_t rk[MMAX];
-  uint32_t ri[MMAX];
-#pragma unroll
-  for (int m = 0; m < MMAX; ++m) {
-    const int e = base + m * 32 + (int)lane;
-    const bool ok = (m * 32 < span) && (e < n);
-    rk[m] = ok ? keys[e] : 0u;
-    ri[m] = ok ? (uint32_t)idx[e] : 0u;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int e = tid; e < n; e += 128) {
+    const uint32_t k = keys[e];
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
   }
-  uint32_t prefix = 0, pmask = 0;
-  int kk = keep;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    ms[MS_MIN + wq] = (int)kmin;
+    ms[MS_MAX + wq] = (int)kmax;
+  }
+  named_bar_sync(bar_id, 128);
+  kmin = min(min((uint32_t)ms[MS_MIN + 0], (uint32_t)ms[MS_MIN + 1]),
+             min((uint32_t)ms[MS_MIN + 2], (uint32_t)ms[MS_MIN + 3]));
+  kmax = max(max((uint32_t)ms[MS_MAX + 0], (uint32_t)ms[MS_MAX + 1]),
+             max((uint32_t)ms[MS_MAX + 2], (uint32_t)ms[MS_MAX + 3]));
+  const uint32_t range = kmax - kmin;
+  const int nbits = range == 0 ? 0 : 32 - __clz(range);
+  int shift = nbits > 8 ? nbits - 8 : 0;
+  uint32_t prefix = 0, pmask = 0;   // in key - kmin space
+  int kk = keep;                    // rank still to place inside the current bin
+  int keep_eq = keep;               // entries of the final bin to keep
+  bool resolved = false;            // prefix is the exact keep-th key
+  for (;;) {
     for (int b = tid; b < 256; b += 128) hist[b] = 0;
     named_bar_sync(bar_id, 128);
-#pragma unroll
-    for (int m = 0; m < MMAX; ++m) {
-      const int e = base + m * 32 + (int)lane;
-      if ((m * 32 < span) && (e < n) && ((rk[m] & pmask) == prefix))
-        atomicAdd(&hist[(rk[m] >> shift) & 0xFFu], 1);
+    for (int e = tid; e < n; e += 128) {
+      const uint32_t rel = keys[e] - kmin;
+      if ((rel & pmask) == prefix) atomicAdd(&hist[(rel >> shift) & 0xFFu], 1);
     }
     named_bar_sync(bar_id, 128);
     const int hi_bin = 255 - 2 * tid;
@@ -264,50 +306,164 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
     const int bin = ms[MS_BIN];
     prefix |= (uint32_t)d << shift;
     pmask |= 0xFFu << shift;
-    if (bin == kk) break;   // the whole bin is kept: threshold found early (uniform)
-  }
-  // stable compaction: keep (key & pmask) > prefix, and the first kk with == prefix
-  int gt = 0, eq = 0;
-#pragma unroll
-  for (int m = 0; m < MMAX; ++m) {
-    const int e = base + m * 32 + (int)lane;
-    const bool v = (m * 32 < span) && (e < n);
-    const uint32_t mk = rk[m] & pmask;
-    gt += __popc(__ballot_sync(0xffffffffu, v && mk > prefix));
-    eq += __popc(__ballot_sync(0xffffffffu, v && mk == prefix));
-  }
-  if (lane == 0) {
-    ms[MS_GT + wq] = gt;
-    ms[MS_EQ + wq] = eq;
-  }
-  named_bar_sync(bar_id, 128);
-  int gbase = 0, ebase = 0;
-  for (int w = 0; w < wq; ++w) {
-    gbase += ms[MS_GT + w];
-    ebase += ms[MS_EQ + w];
-  }
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int m = 0; m < MMAX; ++m) {
-    const int e = base + m * 32 + (int)lane;
-    const bool v = (m * 32 < span) && (e < n);
-    const uint32_t mk = rk[m] & pmask;
-    const bool g1 = v && mk > prefix;
-    const bool e1 = v && mk == prefix;
-    const uint32_t bg = __ballot_sync(0xffffffffu, g1);
-    const uint32_t be = __ballot_sync(0xffffffffu, e1);
-    const int gb = gbase + __popc(bg & lt);
-    const int eb = ebase + __popc(be & lt);
-    if (g1 || (e1 && eb < kk)) {
-      const int pos = gb + (eb < kk ? eb : kk);
-      keys[pos] = rk[m];
-      idx[pos] = (uint16_t)ri[m];
+    if (bin == kk) {                       // the whole bin is kept
+      keep_eq = bin;
+      resolved = shift == 0;
+      break;
     }
-    gbase += __popc(bg);
-    ebase += __popc(be);
+    if (shift == 0) {                      // prefix is the exact keep-th key
+      keep_eq = kk;
+      resolved = true;
+      break;
+    }
+    if (!exact && keep - kk + bin <= cap_after) {
+      keep_eq = bin;
+      break;
+    }
+    shift = shift > 8 ? shift - 8 : 0;
+  }
+  // stable compaction in rounds of 512: keep (rel & pmask) > prefix, and the
+  // first keep_eq (in buffer order) with == prefix
+  const uint32_t lt = (1u << lane) - 1u;
+  int out = 0, eq_seen = 0;
+  for (int r0 = 0, rnd = 0; r0 < n; r0 += 512, ++rnd) {
+    uint32_t rk[4];
+    uint16_t ri[4];
+    uint32_t bg[4], be[4];
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = r0 + wq * 128 + m * 32 + (int)lane;
+      const bool v = e < n;
+      rk[m] = v ? keys[e] : 0u;
+      ri[m] = v ? idx[e] : (uint16_t)0;
+      const uint32_t mk = (rk[m] - kmin) & pmask;
+      bg[m] = __ballot_sync(0xffffffffu, v && mk > prefix);
+      be[m] = __ballot_sync(0xffffffffu, v && mk == prefix);
+      gt += __popc(bg[m]);
+      eq += __popc(be[m]);
+    }
+    int* rc = ms + MS_RCNT + (rnd & 1) * 8;
+    if (lane == 0) {
+      rc[wq] = gt;
+      rc[4 + wq] = eq;
+    }
+    named_bar_sync(bar_id, 128);   // round counts visible; every read of this round done
+    int gb = out, eb = eq_seen, gtot = 0, etot = 0;
+    for (int w = 0; w < 4; ++w) {
+      if (w < wq) {
+        gb += rc[w];
+        eb += rc[4 + w];
+      }
+      gtot += rc[w];
+      etot += rc[4 + w];
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const bool g1 = (bg[m] >> lane) & 1u;
+      const bool e1 = (be[m] >> lane) & 1u;
+      const int my_g = gb + __popc(bg[m] & lt);
+      const int my_e = eb + __popc(be[m] & lt);
+      if (g1 || (e1 && my_e < keep_eq)) {
+        const int pos = my_g + (my_e < keep_eq ? my_e : keep_eq);   // kept entries before it
+        keys[pos] = rk[m];
+        idx[pos] = ri[m];
+      }
+      gb += __popc(bg[m]);
+      eb += __popc(be[m]);
+    }
+    out += gtot;
+    eq_seen += etot;
   }
   named_bar_sync(bar_id, 128);
-  return prefix;
+  *count_out = out + (eq_seen < keep_eq ? eq_seen : keep_eq);
+  const uint32_t edge = kmin + prefix;
+  return resolved ? edge : edge - 1u;
+}
+
+// Approximate shrink from a sample: sort 128 evenly spaced entries
+// (bitonic, descending), take the sample key at the rank that maps to the
+// middle of [keep, cap_after], count the entries >= it exactly, and if that
+// count lies in the window keep exactly those entries (stable, in place).
+// Returns false and changes nothing when the count misses the window (heavy
+// ties, skewed samples); the caller then uses the radix select.  On success
+// *tau_out is the new acceptance threshold (candidate - 1: later keys equal to
+// it are still accepted, so nothing that may belong to the top-k is lost).
+__device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, int n, int keep,
+                                               int cap_after, int wq, uint32_t lane, int* ms,
+                                               int bar_id, uint32_t* tau_out, int* count_out) {
+  const int tid = wq * 32 + (int)lane;
+  uint32_t* sbuf = reinterpret_cast<uint32_t*>(ms + MS_SORT);
+  uint32_t sk = keys[(int)(((long long)tid * n) >> 7)];
+#pragma unroll
+  for (int k2 = 2; k2 <= 128; k2 <<= 1) {
+#pragma unroll
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      uint32_t other;
+      if (j >= 32) {
+        sbuf[tid] = sk;
+        named_bar_sync(bar_id, 128);
+        other = sbuf[tid ^ j];
+        named_bar_sync(bar_id, 128);
+      } else {
+        other = __shfl_xor_sync(0xffffffffu, sk, j);
+      }
+      const bool desc = (tid & k2) == 0;
+      const bool low = (tid & j) == 0;
+      sk = (low == desc) ? max(sk, other) : min(sk, other);
+    }
+  }
+  int r = (int)((((long long)keep + cap_after) / 2 * 128) / n);
+  r = r < 0 ? 0 : (r > 127 ? 127 : r);
+  if (tid == r) ms[MS_CAND] = (int)sk;
+  named_bar_sync(bar_id, 128);
+  const uint32_t cand = (uint32_t)ms[MS_CAND];
+  int c = 0;
+  for (int e = tid; e < n; e += 128) c += keys[e] >= cand ? 1 : 0;
+  c = __reduce_add_sync(0xffffffffu, c);
+  if (lane == 0) ms[MS_CNT4 + wq] = c;
+  named_bar_sync(bar_id, 128);
+  const int total = ms[MS_CNT4 + 0] + ms[MS_CNT4 + 1] + ms[MS_CNT4 + 2] + ms[MS_CNT4 + 3];
+  if (total < keep || total > cap_after) return false;   // uniform: every thread read the same counts
+  // stable compaction in rounds of 512 entries
+  const uint32_t lt = (1u << lane) - 1u;
+  int out = 0;
+  for (int r0 = 0, rnd = 0; r0 < n; r0 += 512, ++rnd) {
+    uint32_t rk[4], bk[4];
+    uint16_t ri[4];
+    int cnt = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = r0 + wq * 128 + m * 32 + (int)lane;
+      const bool v = e < n;
+      rk[m] = v ? keys[e] : 0u;
+      ri[m] = v ? idx[e] : (uint16_t)0;
+      bk[m] = __ballot_sync(0xffffffffu, v && rk[m] >= cand);
+      cnt += __popc(bk[m]);
+    }
+    int* rc = ms + MS_RCNT + (rnd & 1) * 8;
+    if (lane == 0) rc[wq] = cnt;
+    named_bar_sync(bar_id, 128);
+    int base = out, tot = 0;
+    for (int w = 0; w < 4; ++w) {
+      if (w < wq) base += rc[w];
+      tot += rc[w];
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      if ((bk[m] >> lane) & 1u) {
+        const int pos = base + __popc(bk[m] & lt);
+        keys[pos] = rk[m];
+        idx[pos] = ri[m];
+      }
+      base += __popc(bk[m]);
+    }
+    out += tot;
+  }
+  named_bar_sync(bar_id, 128);
+  *count_out = out;
+  *tau_out = cand - 1u;
+  return true;
 }
 
 // ----------------------------------------------------------------------------
@@ -317,6 +473,13 @@ template <int PREC, int H>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_topk_kernel(const __grid_constant__ ScoreParams p) {
   constexpr int QS_MAX = (128 / H) < kMaxQs ? (128 / H) : kMaxQs;
+  constexpr int QPW_MAX = QS_MAX * kG / kEpiWGs;      // queries per epilogue warpgroup
+  constexpr int NCOLW = QPW_MAX * H;                  // accumulator columns a thread reads per tile
+  constexpr int CK = NCOLW < 16 ? NCOLW : 16;         // columns per TMEM load chunk
+  constexpr int GRP = NCOLW < 32 ? NCOLW : 32;        // columns per load/wait group
+  constexpr int NGRP = NCOLW / GRP;
+  constexpr int NCH = (H / 4) < 4 ? (H / 4) : 4;     // independent FFMA2 chains per query
+  static_assert(QPW_MAX >= 1 && QPW_MAX <= kMaxQpw, "queries per warpgroup");
   constexpr bool MX = PREC == PREC_MXFP8;
   const ScorePlan& pl = p.plan;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -348,7 +511,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_tfull(s), 1);
-      mbar_init(bar_tempty(s), 4);
+      mbar_init(bar_tempty(s), 4 * (kEpiWGs / kG));   // every warp of the warpgroups reading it
     }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
@@ -373,10 +536,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
+      PT_DECL
       uint32_t scount = 0;
       int it = 0;
       bool ok = true;
-      const uint32_t q_bytes = kG * pl.chunks * kStageBytes + (MX ? kG * kSfRawWords * 4 : 0);
+      const uint32_t q_bytes = kG * pl.chunks * pl.qchunk + (MX ? kG * kSfRawWords * 4 : 0);
       const uint32_t k_bytes = kStageBytes + (MX ? kSfRawWords * 4 : 0);
       const int chunk_elems = kChunkBytes / (MX ? 1 : 2);
       for (int r = 0; ok && r * G < nitems; ++r) {
@@ -384,15 +548,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (i < 0) continue;
         const Item m = load_item(p, i);
         if (m.ntiles == 0) continue;
+        PT_MARK();
         if (it > 0 && !mbar_wait(bar_qempty, (it - 1) & 1, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
+        PT_ADD(0);
         mbar_arrive_expect_tx(bar_qfull, q_bytes);
         for (int g = 0; g < kG; ++g) {
           const int row = m.qrow0 + g * pl.nsub;
           for (int c = 0; c < pl.chunks; ++c)
-            tma_load_2d(sbase + pl.q_off + (g * pl.chunks + c) * kStageBytes, &p.tm_q, bar_qfull,
+            tma_load_2d(sbase + pl.q_off + (g * pl.chunks + c) * pl.qchunk, &p.tm_q, bar_qfull,
                         c * chunk_elems, row);
           if (MX) tma_load_1d(sbase + pl.sfb_raw_off + g * kSfRawBytes, &p.tm_qs, bar_qfull, row);
         }
@@ -401,11 +567,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const int krow = m.krow0 + t * kTileKeys;
           for (int c = 0; c < pl.chunks; ++c) {
             const int st = scount % nst;
+            PT_MARK();
             if (scount >= (uint32_t)nst &&
                 !mbar_wait(bar_empty(st), ((scount / nst) - 1) & 1, abort_flag, status, tmo)) {
               ok = false;
               break;
             }
+            PT_ADD(1);
             if (p.fault_inject == 1 && scount == 0) {   // test hook: never load stage 0
               ++scount;
               continue;
@@ -429,10 +597,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         if (it > 0) drain_wait(bar_qfull, (it - 1) & 1, tmo);
       }
+      PT_FLUSH(0, true);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
+    PT_DECL
     uint32_t scount = 0, tcount = 0;
     int it = 0;
     bool ok = true;
@@ -443,10 +613,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (i < 0) continue;
       const Item m = load_item(p, i);
       if (m.ntiles == 0) continue;
+      PT_MARK();
       if (!__all_sync(0xffffffffu, mbar_wait(bar_qfull, it & 1, abort_flag, status, tmo))) {
         ok = false;
         break;
       }
+      PT_ADD(0);
       if (MX) {
         for (int g = 0; g < kG; ++g)
           transpose_scales(reinterpret_cast<const uint32_t*>(smem + pl.sfb_raw_off + g * kSfRawBytes),
@@ -463,7 +635,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         __syncwarp();
       }
       for (int t = 0; ok && t < m.ntiles; ++t) {
+        // both sub-block slots of this tile must be free before its MMAs
         uint32_t slot[kG];
+        PT_MARK();
         for (int g = 0; g < kG; ++g) {
           const uint32_t u = tcount * kG + g;
           slot[g] = u % S;
@@ -475,14 +649,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
         }
         if (!ok) break;
+        PT_ADD(1);
         tc_fence_after();
         const int krow = m.krow0 + t * kTileKeys;
         for (int c = 0; c < pl.chunks; ++c) {
           const int st = scount % nst;
+          PT_MARK();
           if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (scount / nst) & 1, abort_flag, status, tmo))) {
             ok = false;
             break;
           }
+          PT_ADD(2);
           if (MX) {
             transpose_scales(
                 reinterpret_cast<const uint32_t*>(smem + pl.sfa_raw_off + st * kSfRawBytes),
@@ -495,10 +672,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_after();
             const uint32_t a_base = sbase + pl.k_off + st * kStageBytes;
             if (MX)
-              tc_cp_32x128b_warpx4(tmem + sfa_col + 4 * (st & 1),
+              tc_cp_32x128b_warpx4(tmem + sfa_col + 4 * (tcount & 1),   // alternates per tile
                                    sf_src_desc(sbase + pl.sfa_tx_off + st * kSfTxBytes));
             for (int g = 0; g < kG; ++g) {
-              const uint32_t b_base = sbase + pl.q_off + (g * pl.chunks + c) * kStageBytes;
+              const uint32_t b_base = sbase + pl.q_off + (g * pl.chunks + c) * pl.qchunk;
               const uint32_t d_tmem = tmem + slot[g] * 128;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
@@ -506,8 +683,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 const uint64_t bd = sw128_kmajor_desc(b_base, kk * 32);
                 const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
                 if (MX)
-                  mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, pl.nsub, kk), tmem + sfa_col + 4 * (st & 1),
-                           tmem + sfb_col + 4 * g, acc);
+                  mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, pl.nsub, kk),
+                           tmem + sfa_col + 4 * (tcount & 1), tmem + sfb_col + 4 * g, acc);
                 else
                   mma_bf16(d_tmem, ad, bd, idesc, acc);
               }
@@ -515,6 +692,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_commit(bar_empty(st));
           }
           __syncwarp();
+          PT_ADD(3);
           ++scount;
         }
         if (!ok) break;
@@ -532,31 +710,40 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc_commit(bar_drain);
       drain_wait(bar_drain, 0, tmo);
     }
+    PT_FLUSH(8, lane == 0);
     __syncwarp();
   } else {
     // ======================= epilogue warpgroups =======================
-    const int g = (warp - kEpiWarp0) >> 2;       // sub-block of this warpgroup
+    // kEpiWGs warpgroups; warpgroup v owns qpw consecutive queries of the item
+    // (one query at 64 heads).  Thread `row` owns key row `row` of each tile.
+    const int v = (warp - kEpiWarp0) >> 2;
     const int wq = warp & 3;                      // TMEM lane quarter = key rows wq*32..
     const int row = wq * 32 + (int)lane;          // key row of the tile owned by this thread
     const int tid = row;                          // thread index inside the warpgroup
-    const int bar_id = 1 + g;
+    const int bar_id = 1 + v;
     const int qs = pl.qs, keep = pl.keep, C = pl.cand, W = p.out_width;
-    uint32_t* ckey_base = reinterpret_cast<uint32_t*>(smem + pl.cand_key_off) + g * qs * C;
-    uint16_t* cidx_base = reinterpret_cast<uint16_t*>(smem + pl.cand_idx_off) + g * qs * C;
-    float* w_s = reinterpret_cast<float*>(smem + pl.w_off) + g * qs * H;
-    int* hist = reinterpret_cast<int*>(smem + pl.hist_off) + g * 256;
-    int* ms = reinterpret_cast<int*>(smem + pl.misc_off) + g * kMiscInts;
+    const int qpw = qs * kG / kEpiWGs;            // queries of this warpgroup
+    const int qpw_eff = QPW_MAX == 1 ? 1 : qpw;   // compile-time when a warpgroup owns one query
+    const int lq0 = v * qpw;                      // first of them, local to the item
+    const int g = lq0 / qs;                       // sub-block = TMEM slot they live in
+    const int col0 = (lq0 - g * qs) * H;          // their first accumulator column
+    uint32_t* ckey_base = reinterpret_cast<uint32_t*>(smem + pl.cand_key_off) + lq0 * C;
+    uint16_t* cidx_base = reinterpret_cast<uint16_t*>(smem + pl.cand_idx_off) + lq0 * C;
+    float* w_s = reinterpret_cast<float*>(smem + pl.w_off) + lq0 * H;
+    int* hist = reinterpret_cast<int*>(smem + pl.hist_off) + v * 256;
+    int* ms = reinterpret_cast<int*>(smem + pl.misc_off) + v * kMiscInts;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t lt = (1u << lane) - 1u;
-    uint32_t tcount = 0;
+    uint32_t tcount = 0, nbatch = 0;
     bool aborted = false;
+    PT_DECL
     for (int r = 0; !aborted && r * G < nitems; ++r) {
       const int i = item_index(r, nitems);
       if (i < 0) continue;
       const Item m = load_item(p, i);
-      const int qbase = m.t0 + g * qs;            // local position of query qi = 0
+      const int qbase = m.t0 + lq0;               // local position of query qi = 0
       const int a = p.cu_seqlens[m.doc];
-      for (int e = tid; e < qs * H; e += 128) {
+      for (int e = tid; e < qpw * H; e += 128) {
         const int t = qbase + e / H;
         float wv = 0.f;
         if (t < m.L) {
@@ -566,103 +753,174 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         w_s[e] = wv;
       }
-      int count[QS_MAX];
-      uint32_t tau[QS_MAX];
+      int count[QPW_MAX];
+      uint32_t tau[QPW_MAX];
+      int vis_lim[QPW_MAX];   // last visible key (or complete pool) of each query; -1 = none
 #pragma unroll
-      for (int qi = 0; qi < QS_MAX; ++qi) {
+      for (int qi = 0; qi < QPW_MAX; ++qi) {
         count[qi] = 0;
         tau[qi] = 0u;
+        const int tq = qbase + qi;
+        vis_lim[qi] = tq >= m.L ? -1 : (p.pool > 1 ? (tq + 1) / p.pool - 1 : tq);
       }
       named_bar_sync(bar_id, 128);
-      for (int t = 0; t < m.ntiles; ++t) {
-        const uint32_t u = tcount * kG + g;
-        const uint32_t slot = u % S;
-        const bool ok = mbar_wait(bar_tfull(slot), (u / S) & 1, abort_flag, status, tmo);
-        tc_fence_after();
-        const int s_idx = t * kTileKeys + row;    // local key (or pool) index of this thread
-        uint32_t key[QS_MAX];
-        bool pass[QS_MAX];
+      PT_ADD(5);
+      for (int tb = 0; tb < m.ntiles; tb += kBatch) {
+        // ---- score kBatch tiles; keep keys and ballots in registers ----
+        uint32_t bkey[kBatch][QPW_MAX];
+        uint32_t bbal[kBatch][QPW_MAX];
+        bool ok_all = true;
 #pragma unroll
-        for (int qi = 0; qi < QS_MAX; ++qi) {
-          pass[qi] = false;
-          key[qi] = 0u;
-          if (qi < qs) {
-            uint32_t acc[H];
-            tmem_load_cols<H>(tmem + lane_base + slot * 128 + qi * H, acc);
-            tmem_ld_wait();
-            const float* wq_s = w_s + qi * H;
-            float2 s2 = make_float2(0.f, 0.f);
+        for (int b = 0; b < kBatch; ++b) {
 #pragma unroll
-            for (int j = 0; j < H; j += 2) {
-              const float2 wv = *reinterpret_cast<const float2*>(wq_s + j);
-              const float2 rv = make_float2(fmaxf(__uint_as_float(acc[j]), 0.f),
-                                            fmaxf(__uint_as_float(acc[j + 1]), 0.f));
-              s2 = ffma2(wv, rv, s2);
+          for (int qi = 0; qi < QPW_MAX; ++qi) {
+            bkey[b][qi] = 0u;
+            bbal[b][qi] = 0u;
+          }
+          const int t = tb + b;
+          if (t < m.ntiles) {
+            const uint32_t u = tcount * kG + g;
+            const uint32_t slot = u % S;
+            ok_all &= mbar_wait(bar_tfull(slot), (u / S) & 1, abort_flag, status, tmo);
+            PT_ADD(0);
+            tc_fence_after();
+            const int s_idx = t * kTileKeys + row;      // local key (or pool) index
+            float2 part[QPW_MAX][NCH];
+#pragma unroll
+            for (int qi = 0; qi < QPW_MAX; ++qi)
+#pragma unroll
+              for (int c = 0; c < NCH; ++c) part[qi][c] = make_float2(0.f, 0.f);
+            // TMEM -> registers in groups of GRP columns (load, wait, reduce), to
+            // keep register pressure low; the slot goes back to the MMA warp as
+            // soon as the last group has landed.  sum_j w_j * ReLU(acc_j) with
+            // NCH independent FFMA2 chains per query.
+            const uint32_t taddr = tmem + lane_base + slot * 128 + col0;
+#pragma unroll
+            for (int gi = 0; gi < NGRP; ++gi) {
+              uint32_t cb[GRP / CK][CK];
+#pragma unroll
+              for (int c = 0; c < GRP / CK; ++c) tmem_load_cols<CK>(taddr + gi * GRP + c * CK, cb[c]);
+#pragma unroll
+              for (int c = 0; c < GRP / CK; ++c) tmem_wait_tied<CK>(cb[c]);
+              if (gi == NGRP - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_tempty(slot));   // slot free for the MMA warp
+                PT_ADD(6);
+              }
+#pragma unroll
+              for (int c = 0; c < GRP / CK; ++c) {
+#pragma unroll
+                for (int j4 = 0; j4 < CK / 4; ++j4) {
+                  const int col = gi * GRP + c * CK + 4 * j4;
+                  const int qi = col / H, hh = col % H;
+                  if (qi < qpw_eff) {
+                    const float4 wv = *reinterpret_cast<const float4*>(w_s + qi * H + hh);
+                    const uint32_t* x = cb[c] + 4 * j4;
+                    const float2 r0 = make_float2(fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
+                    const float2 r1 = make_float2(fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
+                    float2& pc = part[qi][(hh / 4) % NCH];
+                    pc = ffma2(make_float2(wv.x, wv.y), r0, pc);
+                    pc = ffma2(make_float2(wv.z, wv.w), r1, pc);
+                  }
+                }
+              }
             }
-            const float v = (s2.x + s2.y) * p.sm_scale;
-            const int tq = qbase + qi;
-            const bool vis = tq < m.L && (p.pool > 1 ? s_idx < (tq + 1) / p.pool : s_idx <= tq);
-            key[qi] = orderable_key(v);
-            pass[qi] = vis && key[qi] > tau[qi];
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(slot));
-        int* wcnt = ms + MS_WCNT + (tcount & 1) * (kMaxQs * 4);
-        uint32_t bal[QS_MAX];
 #pragma unroll
-        for (int qi = 0; qi < QS_MAX; ++qi) {
-          bal[qi] = 0u;
-          if (qi < qs) {
-            bal[qi] = __ballot_sync(0xffffffffu, pass[qi]);
-            if (lane == 0) wcnt[qi * 4 + wq] = __popc(bal[qi]);
+            for (int qi = 0; qi < QPW_MAX; ++qi) {
+              if (qi < qpw_eff) {
+                float sv = 0.f;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) sv += part[qi][c].x + part[qi][c].y;
+                sv *= p.sm_scale;
+                const bool vis = s_idx <= vis_lim[qi];
+                bkey[b][qi] = orderable_key(sv);
+                bbal[b][qi] = __ballot_sync(0xffffffffu, vis && bkey[b][qi] > tau[qi]);
+              }
+            }
+            ++tcount;
+            PT_ADD(1);
           }
         }
-        if (named_bar_or(bar_id, 128, !ok || *abort_flag)) {
+        // ---- append the batch in index order: one warpgroup barrier ----
+        int* bcnt = ms + MS_BCNT + (nbatch & 1) * (kBatch * kMaxQpw * 4);
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+            for (int qi = 0; qi < QPW_MAX; ++qi) bcnt[(b * kMaxQpw + qi) * 4 + wq] = __popc(bbal[b][qi]);
+        }
+        ++nbatch;
+        named_bar_sync(bar_id, 128);      // batch counts of this warpgroup visible
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+#pragma unroll
+          for (int qi = 0; qi < QPW_MAX; ++qi) {
+            if (qi < qpw) {
+              const int* cc = bcnt + (b * kMaxQpw + qi) * 4;
+              const int c0 = cc[0], c1 = cc[1], c2 = cc[2], c3 = cc[3];
+              const int before = (wq > 0 ? c0 : 0) + (wq > 1 ? c1 : 0) + (wq > 2 ? c2 : 0);
+              if ((bbal[b][qi] >> lane) & 1u) {
+                const int pos = count[qi] + before + __popc(bbal[b][qi] & lt);
+                ckey_base[qi * C + pos] = bkey[b][qi];
+                cidx_base[qi * C + pos] = (uint16_t)((tb + b) * kTileKeys + row);
+              }
+              count[qi] += c0 + c1 + c2 + c3;
+            }
+          }
+        }
+        PT_ADD(2);
+        // ---- room for the next batch, or shrink: all warpgroups together ----
+        // One vote over every epilogue thread decides, uniformly, whether to
+        // abort and whether to shrink; shrinking in lockstep lets the four
+        // queries' compactions overlap instead of stalling the shared TMEM ring
+        // one after another.
+        bool need = false;
+#pragma unroll
+        for (int qi = 0; qi < QPW_MAX; ++qi)
+          need |= qi < qpw && count[qi] + kBatch * kTileKeys > C;
+        const int vote = named_bar_or(kEpiBarAll, kEpiWGs * 128, !ok_all || *abort_flag) ? 2 : 0;
+        if (vote) {
           aborted = true;
           break;
         }
+        if (named_bar_or(kEpiBarAll, kEpiWGs * 128, need)) {
 #pragma unroll
-        for (int qi = 0; qi < QS_MAX; ++qi) {
-          if (qi < qs) {
-            const int c0 = wcnt[qi * 4 + 0], c1 = wcnt[qi * 4 + 1], c2 = wcnt[qi * 4 + 2],
-                      c3 = wcnt[qi * 4 + 3];
-            const int before = (wq > 0 ? c0 : 0) + (wq > 1 ? c1 : 0) + (wq > 2 ? c2 : 0);
-            if (pass[qi]) {
-              const int pos = count[qi] + before + __popc(bal[qi] & lt);
-              ckey_base[qi * C + pos] = key[qi];
-              cidx_base[qi * C + pos] = (uint16_t)s_idx;
+          for (int qi = 0; qi < QPW_MAX; ++qi) {
+            if (qi < qpw && count[qi] > keep + kTileKeys) {
+              named_bar_sync(bar_id, 128);   // appends visible to the whole warpgroup
+              const int cap = C - (kBatch + 2) * kTileKeys;
+              int kept;
+              uint32_t th;
+              if (wg_shrink_sampled(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, cap, wq,
+                                    lane, ms, bar_id, &th, &kept)) {
+                tau[qi] = th;
+              } else {
+                tau[qi] = wg_select(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, false,
+                                    cap, wq, lane, hist, ms, bar_id, &kept);
+              }
+              count[qi] = kept;
             }
-            count[qi] += c0 + c1 + c2 + c3;
           }
         }
-#pragma unroll
-        for (int qi = 0; qi < QS_MAX; ++qi) {
-          if (qi < qs && count[qi] + kTileKeys > C) {
-            named_bar_sync(bar_id, 128);   // appends visible to the whole warpgroup
-            tau[qi] = wg_select<kMaxCand / 128>(ckey_base + qi * C, cidx_base + qi * C, count[qi],
-                                               keep, wq, lane, hist, ms, bar_id);
-            count[qi] = keep;
-          }
-        }
-        ++tcount;
+        PT_ADD(3);
       }
       if (aborted) break;
       named_bar_sync(bar_id, 128);
       // finalize: exactly min(keep, visible) entries per query, ascending index
 #pragma unroll
-      for (int qi = 0; qi < QS_MAX; ++qi) {
-        if (qi < qs && count[qi] > keep) {
-          wg_select<kMaxCand / 128>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, wq,
-                                    lane, hist, ms, bar_id);
-          count[qi] = keep;
+      for (int qi = 0; qi < QPW_MAX; ++qi) {
+        if (qi < qpw && count[qi] > keep) {
+          int kept;
+          wg_select(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, true,
+                                    keep, wq, lane, hist, ms, bar_id, &kept);
+          count[qi] = kept;
         }
       }
 #pragma unroll
-      for (int qi = 0; qi < QS_MAX; ++qi) {
+      for (int qi = 0; qi < QPW_MAX; ++qi) {
         const int tq = qbase + qi;
-        if (qi >= qs || tq >= m.L) continue;
+        if (qi >= qpw || tq >= m.L) continue;
         const size_t orow = (size_t)(a + tq) * W;
         const int n = count[qi];
         const uint32_t* ck = ckey_base + qi * C;
@@ -687,15 +945,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (tid == 0 && p.out_len) p.out_len[a + tq] = n * P + ntail;
         } else {
           for (int e = tid; e < W; e += 128) {
-            const bool v = e < n;
-            p.out_idx[orow + e] = v ? (int)ci[e] : -1;
-            if (p.out_score) p.out_score[orow + e] = v ? key_to_float(ck[e]) : -__int_as_float(0x7f800000);
+            const bool vv = e < n;
+            p.out_idx[orow + e] = vv ? (int)ci[e] : -1;
+            if (p.out_score) p.out_score[orow + e] = vv ? key_to_float(ck[e]) : -__int_as_float(0x7f800000);
           }
           if (tid == 0 && p.out_len) p.out_len[a + tq] = n;
         }
       }
       named_bar_sync(bar_id, 128);
+      PT_ADD(4);
     }
+    PT_FLUSH(16 + 8 * v, tid == 0);
   }
   tc_fence_before();
   __syncthreads();
@@ -859,5 +1119,15 @@ cudaError_t launch_debug_mma_tile(const DebugParams& p, int prec, cudaStream_t s
   }
   return cudaGetLastError();
 }
+
+#ifdef DSA_PHASE_TIMERS
+extern "C" void dsa_idx_debug_phase_timers(unsigned long long* out64, int reset) {
+  cudaMemcpyFromSymbol(out64, g_phase_cycles, sizeof(unsigned long long) * 64);
+  if (reset) {
+    unsigned long long z[64] = {0};
+    cudaMemcpyToSymbol(g_phase_cycles, z, sizeof(z));
+  }
+}
+#endif
 
 }  // namespace dsa
