@@ -201,6 +201,31 @@ dsa_status_t dsa_idx_score_topk(
     int32_t* topk_idx, float* topk_score, int32_t* topk_len,
     void* ws, size_t ws_bytes, dsa_stream_t stream);
 
+/* Allocation-free dsa_idx_score_topk, for callers that cannot provide device
+ * scratch memory: code that runs after a no-allocation-past-start-up point
+ * (latency-critical serving loops, real-time pipelines), hosts whose device
+ * memory belongs to an allocator they may not grow, and plugin-style
+ * integrations that only receive input and output tensors.  The pages describe
+ * no counterpart; it exists for those callers.
+ * Same arguments and results as dsa_idx_score_topk without ws/ws_bytes.  The
+ * scratch lives in a fixed 4 MiB device array inside the library, which every
+ * GPU that loads the library holds until the process exits; sizes whose
+ * dsa_idx_workspace_size exceeds 4 MiB (roughly total_tokens + num_seqs above
+ * 520000) are rejected with DSA_ERR_WORKSPACE before anything is launched.
+ * It calls no cudaMalloc/cudaFree.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before capturing any stream.  All calls share the one
+ * array, so calls whose GPU work overlaps (other streams, or unordered calls
+ * from several host threads) race on it; the device status word of the last
+ * call is not readable through this entry point. */
+dsa_status_t dsa_idx_score_topk_noalloc(
+    const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
+    const void* w, dsa_dtype_t w_dtype, float sm_scale,
+    const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+    int n_heads, int head_dim, int index_topk, dsa_precision_t prec, int flags,
+    int kpool_size, const int32_t* cu_pools,
+    int32_t* topk_idx, float* topk_score, int32_t* topk_len, dsa_stream_t stream);
+
 /* Synchronise `stream` and return the device status word recorded in `ws` by
  * the last dsa_idx_score_topk call on it (DSA_OK if none).  Eager helper; do
  * not call it while capturing a graph. */

@@ -23,6 +23,15 @@ namespace {
 
 thread_local std::string g_last_error;
 
+}  // namespace
+
+namespace dsa {
+// Set the message dsa_idx_last_error() returns (for entry points in other files).
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace dsa
+
+namespace {
+
 dsa_status_t fail(dsa_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 dsa_status_t fail(dsa_status_t s, const char* fmt, ...) {
   char buf[512];
