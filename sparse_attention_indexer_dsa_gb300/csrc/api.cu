@@ -125,12 +125,20 @@ dsa_status_t make_scale_map(CUtensorMap* m, const void* base, int64_t rows) {
 
 bool heads_ok(int H) { return H == 4 || H == 8 || H == 16 || H == 32 || H == 64; }
 
-// workspace layout: [0,256) header (status, item count); doc prefix
-// int[num_seqs+1]; work items int2[total_tokens + num_seqs]
+// workspace layout: [0,256) header (status, item count); per-document item
+// prefix int[num_seqs+1]; per-document key-tile prefix int[num_seqs+1]; work
+// items int2[total_tokens + num_seqs]; MXFP8 only: key scales laid out per
+// key tile, 512 bytes x (total_tokens/128 + num_seqs + 1).
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 size_t ws_prefix_off() { return 256; }
-size_t ws_items_off(int num_seqs) { return 256 + (((size_t)(num_seqs + 1) * 4 + 255) / 256) * 256; }
-size_t ws_total(int total_tokens, int num_seqs) {
-  return ws_items_off(num_seqs) + (size_t)8 * ((size_t)total_tokens + num_seqs);
+size_t ws_tiles_off(int num_seqs) { return ws_prefix_off() + round256((size_t)(num_seqs + 1) * 4); }
+size_t ws_items_off(int num_seqs) { return ws_tiles_off(num_seqs) + round256((size_t)(num_seqs + 1) * 4); }
+size_t ws_ksf_off(int total_tokens, int num_seqs) {
+  return ws_items_off(num_seqs) + round256((size_t)8 * ((size_t)total_tokens + num_seqs));
+}
+int ws_ksf_tiles(int total_tokens, int num_seqs) { return total_tokens / kTileKeys + num_seqs + 1; }
+size_t ws_total(int total_tokens, int num_seqs, bool mx) {
+  return ws_ksf_off(total_tokens, num_seqs) + (mx ? (size_t)kSfTxBytes * ws_ksf_tiles(total_tokens, num_seqs) : 0);
 }
 
 unsigned long long g_timeout_ns = 2000000000ull;
@@ -158,9 +166,9 @@ const char* dsa_idx_status_string(dsa_status_t s) {
 
 size_t dsa_idx_workspace_size(int total_tokens, int num_seqs, int max_seqlen, int n_heads,
                               int head_dim, int index_topk, int kpool_size, dsa_precision_t prec) {
-  (void)max_seqlen; (void)n_heads; (void)head_dim; (void)index_topk; (void)kpool_size; (void)prec;
+  (void)max_seqlen; (void)n_heads; (void)head_dim; (void)index_topk; (void)kpool_size;
   if (total_tokens < 0 || num_seqs < 1) return 0;
-  return ws_total(total_tokens, num_seqs);
+  return ws_total(total_tokens, num_seqs, prec == DSA_PREC_MXFP8);
 }
 
 int dsa_idx_output_width(int index_topk, int kpool_size, int flags) {
@@ -296,8 +304,9 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   const int keep = index_topk / kpool_size;
   if (keep < 1) return fail(DSA_ERR_INVALID_ARG, "index_topk / kpool_size must be >= 1");
   if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
-  if (ws_bytes < ws_total(total_tokens, num_seqs))
-    return fail(DSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, ws_total(total_tokens, num_seqs));
+  const bool mxw = prec == DSA_PREC_MXFP8;
+  if (ws_bytes < ws_total(total_tokens, num_seqs, mxw))
+    return fail(DSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, ws_total(total_tokens, num_seqs, mxw));
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(DSA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   ScoreParams p{};
   const int pl_prec = prec == DSA_PREC_MXFP8 ? PREC_MXFP8 : PREC_BF16;
@@ -308,7 +317,7 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   if (s != DSA_OK) return s;
   const bool fp8 = pl_prec == PREC_MXFP8;
   const int64_t krows = kpool_size > 1 ? total_tokens / kpool_size : total_tokens;
-  if ((s = make_operand_map(&p.tm_q, q, (int64_t)total_tokens * n_heads, head_dim, fp8, p.plan.nsub)) != DSA_OK)
+  if ((s = make_operand_map(&p.tm_q, q, (int64_t)total_tokens * n_heads, head_dim, fp8, p.plan.ncols)) != DSA_OK)
     return s;
   if ((s = make_operand_map(&p.tm_k, k, krows, head_dim, fp8)) != DSA_OK) return s;
   if (fp8) {
@@ -318,8 +327,10 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
   int* hdr = reinterpret_cast<int*>(wsb);
   int* doc_prefix = reinterpret_cast<int*>(wsb + ws_prefix_off());
+  int* tile_base = reinterpret_cast<int*>(wsb + ws_tiles_off(num_seqs));
   int2* items = reinterpret_cast<int2*>(wsb + ws_items_off(num_seqs));
-  const int tq = kG * p.plan.qs;
+  uint32_t* ksf_tiles = reinterpret_cast<uint32_t*>(wsb + ws_ksf_off(total_tokens, num_seqs));
+  const int tq = p.plan.nq;
   const int max_items = total_tokens + num_seqs;
   p.w = w;
   p.cu_seqlens = cu_seqlens;
@@ -329,6 +340,8 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   p.out_len = topk_len;
   p.items = items;
   p.hdr = hdr;
+  p.tile_base = tile_base;
+  p.ksf_tiles = fp8 ? ksf_tiles : nullptr;
   p.timeout_ns = g_timeout_ns;
   p.sm_scale = sm_scale;
   p.w_bf16 = w_dtype == DSA_DTYPE_BF16;
@@ -338,9 +351,14 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   p.fault_inject = g_fault_inject;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_build_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, tq, kpool_size,
-                                        items, doc_prefix, hdr, max_items, st);
+                                        items, doc_prefix, tile_base, hdr, max_items, st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   if (total_tokens == 0) return DSA_OK;
+  if (fp8) {
+    e = launch_tiled_kscales(k_scale, krows, p.cu_keys, tile_base, num_seqs,
+                             ws_ksf_tiles(total_tokens, num_seqs), ksf_tiles, di.sm_count, st);
+    if (e != cudaSuccess) return cuda_fail(e, "key-scale layout launch");
+  }
   int grid = di.sm_count;
   const int64_t bound = (int64_t)total_tokens / tq + num_seqs;
   if (bound < grid) grid = (int)bound;

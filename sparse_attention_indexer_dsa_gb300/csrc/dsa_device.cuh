@@ -127,6 +127,15 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// Non-tensor bulk copy global -> this CTA's shared memory (16-byte aligned
+// addresses, size a multiple of 16), completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // generic-proxy smem writes -> visible to the async proxy (tcgen05.cp / UMMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -40,8 +40,11 @@ cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const 
                          const int32_t* cu, int num_seqs, int total_tokens, int D, int P,
                          uint16_t* out, int32_t* cu_pools, int sm_count, cudaStream_t stream);
 cudaError_t launch_build_worklist(const int32_t* cu, int num_seqs, int total_tokens, int max_seqlen,
-                                  int tq, int pool, int2* items, int* doc_prefix, int* hdr,
-                                  int max_items, cudaStream_t stream);
+                                  int tq, int pool, int2* items, int* doc_prefix, int* tile_base,
+                                  int* hdr, int max_items, cudaStream_t stream);
+cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const int32_t* cu_keys,
+                                 const int* tile_base, int num_seqs, int max_tiles, uint32_t* out,
+                                 int sm_count, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_debug_mma_tile(const DebugParams& p, int prec, cudaStream_t stream);
 

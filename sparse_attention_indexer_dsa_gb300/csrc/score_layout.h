@@ -9,10 +9,8 @@ namespace dsa {
 
 enum { PREC_BF16 = 0, PREC_MXFP8 = 1 };
 
-constexpr int kEpiWGs = 4;           // epilogue warpgroups
-constexpr int kScoreThreads = 64 + 128 * kEpiWGs;   // warp 0: TMA, warp 1: MMA + TMEM, then epilogue
-constexpr int kEpiWarp0 = 2;
-constexpr int kG = 2;                // query sub-blocks (UMMA B operands) per work item
+constexpr int kEpiWarp0 = 2;         // warp 0: TMA producer, warp 1: MMA + TMEM owner, then epilogue
+constexpr int kMaxEpiWGs = 4;
 constexpr int kTileKeys = 128;       // keys per tcgen05 tile (UMMA M)
 constexpr int kChunkBytes = 128;     // bytes of one K-major row per smem chunk (128B swizzle)
 constexpr int kStageBytes = kTileKeys * kChunkBytes;   // 16 KiB
@@ -23,22 +21,35 @@ constexpr int kMaxSmem = 232448;     // 227 KiB opt-in per block on sm_100/sm_10
 constexpr int kMiscInts = 320;       // per-warpgroup scratch ints
 constexpr int kBatch = 4;            // key tiles scored between two appends
 constexpr int kMaxQpw = 4;           // queries per epilogue warpgroup (at most)
-constexpr int kEpiBarAll = 1 + kEpiWGs;   // named barrier of all epilogue warps (1..kEpiWGs: per warpgroup)
 constexpr int kMaxStages = 6;
-constexpr int kMaxQs = 8;
 constexpr int kMaxCand = 4096;
+constexpr int kSfaCol = 384;         // MXFP8: key scales, 2 x 4 TMEM columns (alternating per tile)
+constexpr int kSfbCol = 392;         // MXFP8: query scales, up to 2 atoms x 4 columns
+
+// Per precision: the accumulator of one key tile is ncols <= max_ncols columns
+// of TMEM, double buffered (BF16: 2 x 256; MXFP8: 2 x 192 + 16 scale columns),
+// and one epilogue warpgroup serves each group of qpw queries.
+__host__ __device__ constexpr int max_ncols(int prec) { return prec == PREC_BF16 ? 256 : 192; }
+__host__ __device__ constexpr int epi_wgs(int prec) { return prec == PREC_BF16 ? 4 : 3; }
+__host__ __device__ constexpr int score_threads(int prec) { return 64 + 128 * epi_wgs(prec); }
+__host__ __device__ constexpr int qpw_max(int prec, int n_heads) {
+  return max_ncols(prec) / (epi_wgs(prec) * n_heads) < kMaxQpw ? max_ncols(prec) / (epi_wgs(prec) * n_heads)
+                                                                : kMaxQpw;
+}
 
 // Sizes of one launch of the fused kernel (decided on the host).
 struct ScorePlan {
   int prec, head_dim, n_heads;
-  int qs;        // queries per sub-block
-  int nsub;      // qs * n_heads: UMMA N of one sub-block
+  int ewgs;      // epilogue warpgroups
+  int qpw;       // queries per epilogue warpgroup
+  int nq;        // queries per work item (ewgs * qpw)
+  int ncols;     // nq * n_heads: UMMA N, TMEM columns of one accumulator slot
   int cand;      // candidate-buffer capacity per query (multiple of 128)
   int keep;      // entries kept per query (index_topk, or index_topk / pool size)
   int nst;       // K-tile smem stages
   int chunks;    // 128-byte chunks per operand row: head_dim*elem/128
-  int tslots;    // TMEM accumulator slots of 128 columns
-  int qchunk;    // bytes of one q-operand chunk: nsub rows x 128 bytes (TMA box of the q map)
+  int qchunk;    // bytes of one q-operand chunk: ncols rows x 128 bytes (TMA box of the q map)
+  int sfb_atoms; // MXFP8: 128-row groups of query scales (ceil(ncols / 128))
   // byte offsets into dynamic shared memory (base 1024-aligned)
   int q_off, k_off, sfa_raw_off, sfa_tx_off, sfb_raw_off, sfb_tx_off;
   int cand_key_off, cand_idx_off, w_off, hist_off, misc_off, bar_off, total;
@@ -58,6 +69,8 @@ struct ScoreParams {
   int32_t* out_len;
   const int2* items;        // device work list
   int* hdr;                 // [0] status, [1] item count
+  const int* tile_base;     // first key tile of each document in ksf_tiles
+  const uint32_t* ksf_tiles;   // MXFP8: key scales laid out per key tile for tcgen05.cp (512 B each)
   unsigned long long timeout_ns;
   float sm_scale;
   int w_bf16;
@@ -76,57 +89,53 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
   s.head_dim = head_dim;
   s.n_heads = n_heads;
   s.keep = keep;
+  s.ewgs = epi_wgs(prec);
   const int elem = prec == PREC_BF16 ? 2 : 1;
+  const bool sf = prec == PREC_MXFP8;
   s.chunks = head_dim * elem / kChunkBytes;
-  s.tslots = prec == PREC_BF16 ? 4 : 3;
-  int qs = 128 / n_heads;
-  if (qs > kMaxQs) qs = kMaxQs;
   const int cand_min = keep + (kBatch + 2) * kTileKeys;   // a full batch fits after a shrink
+  int qpw = qpw_max(prec, n_heads);
   int cand = round_up(keep * 2 > cand_min ? keep * 2 : cand_min, 128);
   if (cand > kMaxCand) cand = round_up(cand_min, 128);
-  if (cand > kMaxCand) return false;
+  if (cand > kMaxCand || qpw < 1) return false;
   for (;;) {
-    if (qs * n_heads < 16 || (qs * kG) % kEpiWGs != 0) return false;
-    s.qs = qs;
-    s.nsub = qs * n_heads;
+    s.qpw = qpw;
+    s.nq = s.ewgs * qpw;
+    s.ncols = s.nq * n_heads;
+    if (s.ncols < 16 || s.ncols % 16 != 0 || s.ncols > max_ncols(prec)) return false;
     s.cand = cand;
-    s.qchunk = s.nsub * kChunkBytes;   // a multiple of 1024 (nsub % 16 == 0): keeps the swizzle atoms aligned
-    // fixed part
+    s.qchunk = s.ncols * kChunkBytes;   // multiple of 1024: keeps the swizzle atoms aligned
+    s.sfb_atoms = sf ? (s.ncols + 127) / 128 : 0;
     int off = 0;
     s.q_off = off;
-    off += kG * s.chunks * s.qchunk;
+    off += s.chunks * s.qchunk;
     s.k_off = off;
-    // the rest, independent of the stage count
-    int rest = 0;
-    const int sf = prec == PREC_MXFP8;
-    int cand_bytes = kG * qs * cand * 6;
-    rest += cand_bytes + kG * qs * n_heads * 4 + kEpiWGs * 256 * 4 + kEpiWGs * kMiscInts * 4 + 512;
-    int per_stage = kStageBytes + (sf ? kSfRawBytes + kSfTxBytes : 0);
-    int sfb = sf ? kG * (kSfRawBytes + kSfTxBytes) : 0;
+    const int rest = s.nq * cand * 6 + s.nq * n_heads * 4 + s.ewgs * 256 * 4 + s.ewgs * kMiscInts * 4 + 512 + 64;
+    const int per_stage = kStageBytes + (sf ? kSfTxBytes : 0);
+    const int sfb = sf ? 2 * (kSfRawBytes + kSfTxBytes) : 0;
     int nst = (kMaxSmem - 1024 - off - rest - sfb) / per_stage;
     if (nst > kMaxStages) nst = kMaxStages;
     if (nst >= 2) {
       s.nst = nst;
       off += nst * kStageBytes;
-      s.sfa_raw_off = off;
-      off += sf ? nst * kSfRawBytes : 0;
+      s.sfa_raw_off = off;   // unused: key scales arrive already laid out for tcgen05.cp
       s.sfa_tx_off = off;
       off += sf ? nst * kSfTxBytes : 0;
       s.sfb_raw_off = off;
-      off += sf ? kG * kSfRawBytes : 0;
+      off += sf ? 2 * kSfRawBytes : 0;
       s.sfb_tx_off = off;
-      off += sf ? kG * kSfTxBytes : 0;
+      off += sf ? 2 * kSfTxBytes : 0;
       s.cand_key_off = off;
-      off += kG * qs * cand * 4;
+      off += s.nq * cand * 4;
       s.cand_idx_off = off;
-      off += kG * qs * cand * 2;
+      off += s.nq * cand * 2;
       off = round_up(off, 16);
       s.w_off = off;
-      off += kG * qs * n_heads * 4;
+      off += s.nq * n_heads * 4;
       s.hist_off = off;
-      off += kEpiWGs * 256 * 4;
+      off += s.ewgs * 256 * 4;
       s.misc_off = off;
-      off += kEpiWGs * kMiscInts * 4;
+      off += s.ewgs * kMiscInts * 4;
       off = round_up(off, 8);
       s.bar_off = off;
       off += 512;
@@ -138,8 +147,8 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
       cand = round_up(cand_min, 128);
       continue;
     }
-    if (qs > 2 && (qs / 2) * n_heads >= 16) {   // qs stays even: kG*qs splits over kEpiWGs
-      qs /= 2;
+    if (qpw > 1) {
+      qpw /= 2;
       cand = round_up(keep * 2 > cand_min ? keep * 2 : cand_min, 128);
       if (cand > kMaxCand) cand = round_up(cand_min, 128);
       continue;

@@ -47,6 +47,14 @@ __device__ unsigned long long g_phase_cycles[64];
 #define PT_ADD(i) ((void)0)
 #define PT_FLUSH(base, rec) ((void)0)
 #endif
+// Optional event timeline of CTA 0 (compile with -DDSA_TRACE): clock64() of
+// event `ev` for tile number `t` (t < 256).
+#ifdef DSA_TRACE
+__device__ long long g_trace[16][256];
+#define TRACE(ev, t, cond) do { if ((cond) && blockIdx.x == 0 && (t) < 256) g_trace[ev][t] = clock64(); } while (0)
+#else
+#define TRACE(ev, t, cond) ((void)0)
+#endif
 
 // ----------------------------------------------------------------------------
 // Work list: items (document, first query) sorted by descending tile count so
@@ -57,8 +65,8 @@ constexpr int kWLMaxBins = 1025;
 
 __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
     const int32_t* __restrict__ cu, int num_seqs, int total_tokens, int max_seqlen, int tq,
-    int pool, int2* __restrict__ items, int* __restrict__ doc_prefix, int* __restrict__ hdr,
-    int max_items) {
+    int pool, int2* __restrict__ items, int* __restrict__ doc_prefix, int* __restrict__ tile_base,
+    int* __restrict__ hdr, int max_items) {
   __shared__ int hist[kWLMaxBins];
   __shared__ int s_bad;
   __shared__ int s_total;
@@ -108,6 +116,32 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
     s_total = carry;
   }
   __syncthreads();
+  // key tiles of every document -> exclusive prefix (where its laid-out key scales start)
+  carry = 0;
+  for (int base = 0; base < num_seqs; base += kWLThreads) {
+    const int d = base + tid;
+    int v = 0;
+    if (d < num_seqs) {
+      const int L = cu[d + 1] - cu[d];
+      v = ((pool > 1 ? L / pool : L) + kTileKeys - 1) / kTileKeys;
+    }
+    int x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((tid & 31) >= o) x += y;
+    }
+    if ((tid & 31) == 31) warp_tot[tid >> 5] = x;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < (tid >> 5); ++w) before += warp_tot[w];
+    if (d < num_seqs) tile_base[d] = carry + before + x - v;
+    int chunk_total = 0;
+    for (int w = 0; w < 32; ++w) chunk_total += warp_tot[w];
+    __syncthreads();
+    carry += chunk_total;
+  }
+  if (tid == 0) tile_base[num_seqs] = carry;
+  __syncthreads();
   const int total = s_total < max_items ? s_total : max_items;
   __threadfence_block();
   auto doc_of = [&](int i) {
@@ -149,11 +183,31 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
   if (tid == 0) hdr[1] = total;
 }
 
+// MXFP8 key scales, laid out once per call in the tcgen05.cp source form: for
+// key tile t of document d (512 bytes at tile_base[d] + t), 16-byte row l holds
+// the 32-bit scale words of the tile's key rows l, l+32, l+64, l+96 (rows past
+// the end of the key tensor get 0).  One thread per (tile, row).
+__global__ void __launch_bounds__(128) build_tiled_kscales_kernel(
+    const uint32_t* __restrict__ kscale_words, int64_t k_rows, const int32_t* __restrict__ cu_keys,
+    const int* __restrict__ tile_base, int num_seqs, int max_tiles, uint32_t* __restrict__ out) {
+  const int total = tile_base[num_seqs];
+  const int r = threadIdx.x;
+  for (int g = blockIdx.x; g < total && g < max_tiles; g += gridDim.x) {
+    int lo = 0, hi = num_seqs - 1;   // document whose tiles contain g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_base[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    const int64_t row = (int64_t)cu_keys[lo] + (int64_t)(g - tile_base[lo]) * kTileKeys + r;
+    out[(size_t)g * 128 + (r & 31) * 4 + (r >> 5)] = row < k_rows ? __ldg(kscale_words + row) : 0u;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // helpers of the fused kernel
 // ----------------------------------------------------------------------------
 struct Item {
-  int doc, t0, L, qrow0, krow0, ntiles;
+  int doc, t0, L, qrow0, krow0, ntiles, ktile0;
 };
 
 __device__ __forceinline__ int item_index(int r, int nitems) {
@@ -172,10 +226,11 @@ __device__ __forceinline__ Item load_item(const ScoreParams& p, int i) {
   m.L = p.cu_seqlens[m.doc + 1] - a;
   m.qrow0 = (a + m.t0) * p.plan.n_heads;
   m.krow0 = p.cu_keys[m.doc];
-  int t_end = m.t0 + kG * p.plan.qs;
+  int t_end = m.t0 + p.plan.nq;
   if (t_end > m.L) t_end = m.L;
   const int nk = p.pool > 1 ? t_end / p.pool : t_end;
   m.ntiles = (nk + kTileKeys - 1) / kTileKeys;
+  m.ktile0 = p.ksf_tiles ? p.tile_base[m.doc] : 0;
   return m;
 }
 
@@ -470,17 +525,17 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
 // the fused kernel
 // ----------------------------------------------------------------------------
 template <int PREC, int H>
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __launch_bounds__(score_threads(PREC), 1)
     score_topk_kernel(const __grid_constant__ ScoreParams p) {
-  constexpr int QS_MAX = (128 / H) < kMaxQs ? (128 / H) : kMaxQs;
-  constexpr int QPW_MAX = QS_MAX * kG / kEpiWGs;      // queries per epilogue warpgroup
+  constexpr bool MX = PREC == PREC_MXFP8;
+  constexpr int EW = epi_wgs(PREC);                   // epilogue warpgroups
+  constexpr int QPW_MAX = qpw_max(PREC, H);           // queries per epilogue warpgroup
   constexpr int NCOLW = QPW_MAX * H;                  // accumulator columns a thread reads per tile
-  constexpr int CK = NCOLW < 16 ? NCOLW : 16;         // columns per TMEM load chunk
-  constexpr int GRP = NCOLW < 32 ? NCOLW : 32;        // columns per load/wait group
+  constexpr int CK = NCOLW < 16 ? NCOLW : 16;         // columns per TMEM load instruction
+  constexpr int GRP = (score_threads(PREC) <= 448 || NCOLW < 32) ? NCOLW : 32;   // columns per load/wait group
   constexpr int NGRP = NCOLW / GRP;
   constexpr int NCH = (H / 4) < 4 ? (H / 4) : 4;     // independent FFMA2 chains per query
   static_assert(QPW_MAX >= 1 && QPW_MAX <= kMaxQpw, "queries per warpgroup");
-  constexpr bool MX = PREC == PREC_MXFP8;
   const ScorePlan& pl = p.plan;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -491,16 +546,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   // barriers
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pl.bar_off);
-  const int nst = pl.nst, S = pl.tslots;
+  const int nst = pl.nst;
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return smem_u32(bars + kMaxStages + s); };
   auto bar_tfull = [&](int s) { return smem_u32(bars + 2 * kMaxStages + s); };
-  auto bar_tempty = [&](int s) { return smem_u32(bars + 2 * kMaxStages + 4 + s); };
-  const uint32_t bar_qfull = smem_u32(bars + 2 * kMaxStages + 8);
-  const uint32_t bar_qempty = smem_u32(bars + 2 * kMaxStages + 9);
-  const uint32_t bar_drain = smem_u32(bars + 2 * kMaxStages + 10);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 12);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 13);
+  auto bar_tempty = [&](int s) { return smem_u32(bars + 2 * kMaxStages + 2 + s); };
+  const uint32_t bar_qfull = smem_u32(bars + 2 * kMaxStages + 4);
+  const uint32_t bar_qempty = smem_u32(bars + 2 * kMaxStages + 5);
+  const uint32_t bar_drain = smem_u32(bars + 2 * kMaxStages + 6);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 9);
   int* status = p.hdr;
   const uint64_t tmo = p.timeout_ns;
 
@@ -509,9 +564,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar_tfull(s), 1);
-      mbar_init(bar_tempty(s), 4 * (kEpiWGs / kG));   // every warp of the warpgroups reading it
+      mbar_init(bar_tempty(s), 4 * EW);   // every epilogue warp reads every tile
     }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
@@ -537,11 +592,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // ======================= TMA producer =======================
     if (lane == 0) {
       PT_DECL
-      uint32_t scount = 0;
+      uint32_t scount = 0, st = 0, ph = 0;
+      bool wrapped = false;
       int it = 0;
       bool ok = true;
-      const uint32_t q_bytes = kG * pl.chunks * pl.qchunk + (MX ? kG * kSfRawWords * 4 : 0);
-      const uint32_t k_bytes = kStageBytes + (MX ? kSfRawWords * 4 : 0);
+      const uint32_t q_bytes = pl.chunks * pl.qchunk + (MX ? pl.sfb_atoms * kSfRawWords * 4 : 0);
+      const uint32_t k_bytes = kStageBytes + (MX ? kSfTxBytes : 0);
       const int chunk_elems = kChunkBytes / (MX ? 1 : 2);
       for (int r = 0; ok && r * G < nitems; ++r) {
         const int i = item_index(r, nitems);
@@ -555,36 +611,36 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         PT_ADD(0);
         mbar_arrive_expect_tx(bar_qfull, q_bytes);
-        for (int g = 0; g < kG; ++g) {
-          const int row = m.qrow0 + g * pl.nsub;
-          for (int c = 0; c < pl.chunks; ++c)
-            tma_load_2d(sbase + pl.q_off + (g * pl.chunks + c) * pl.qchunk, &p.tm_q, bar_qfull,
-                        c * chunk_elems, row);
-          if (MX) tma_load_1d(sbase + pl.sfb_raw_off + g * kSfRawBytes, &p.tm_qs, bar_qfull, row);
-        }
+        for (int c = 0; c < pl.chunks; ++c)
+          tma_load_2d(sbase + pl.q_off + c * pl.qchunk, &p.tm_q, bar_qfull, c * chunk_elems, m.qrow0);
+        if (MX)
+          for (int a = 0; a < pl.sfb_atoms; ++a)
+            tma_load_1d(sbase + pl.sfb_raw_off + a * kSfRawBytes, &p.tm_qs, bar_qfull, m.qrow0 + 128 * a);
         ++it;
         for (int t = 0; ok && t < m.ntiles; ++t) {
           const int krow = m.krow0 + t * kTileKeys;
           for (int c = 0; c < pl.chunks; ++c) {
-            const int st = scount % nst;
             PT_MARK();
-            if (scount >= (uint32_t)nst &&
-                !mbar_wait(bar_empty(st), ((scount / nst) - 1) & 1, abort_flag, status, tmo)) {
+            if (wrapped && !mbar_wait(bar_empty(st), ph ^ 1u, abort_flag, status, tmo)) {
               ok = false;
               break;
             }
             PT_ADD(1);
-            if (p.fault_inject == 1 && scount == 0) {   // test hook: never load stage 0
-              ++scount;
-              continue;
+            if (!(p.fault_inject == 1 && scount == 0)) {   // test hook: stage 0 is never loaded
+              mbar_arrive_expect_tx(bar_full(st), k_bytes);
+              tma_load_2d(sbase + pl.k_off + st * kStageBytes, &p.tm_k, bar_full(st),
+                          c * chunk_elems, krow);
+              if (MX)
+                bulk_load(sbase + pl.sfa_tx_off + st * kSfTxBytes,
+                          p.ksf_tiles + (size_t)(m.ktile0 + t) * (kSfTxBytes / 4), kSfTxBytes,
+                          bar_full(st));
             }
-            mbar_arrive_expect_tx(bar_full(st), k_bytes);
-            tma_load_2d(sbase + pl.k_off + st * kStageBytes, &p.tm_k, bar_full(st),
-                        c * chunk_elems, krow);
-            if (MX)
-              tma_load_1d(sbase + pl.sfa_raw_off + st * kSfRawBytes, &p.tm_ks, bar_full(st),
-                          krow & ~3);
             ++scount;
+            if (++st == nst) {
+              st = 0;
+              ph ^= 1u;
+              wrapped = true;
+            }
           }
         }
       }
@@ -602,12 +658,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
+    // One MMA chain per key tile covering every query of the item (N = ncols),
+    // into TMEM slot tcount & 1 (double buffered).
     PT_DECL
-    uint32_t scount = 0, tcount = 0;
+    uint32_t tcount = 0, st = 0, ph = 0;
     int it = 0;
     bool ok = true;
-    const uint32_t idesc = MX ? 0u : idesc_bf16(128, pl.nsub);
-    const uint32_t sfa_col = 384, sfb_col = 392;
+    const uint32_t idesc = MX ? 0u : idesc_bf16(128, pl.ncols);
     for (int r = 0; ok && r * G < nitems; ++r) {
       const int i = item_index(r, nitems);
       if (i < 0) continue;
@@ -620,84 +677,71 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       PT_ADD(0);
       if (MX) {
-        for (int g = 0; g < kG; ++g)
-          transpose_scales(reinterpret_cast<const uint32_t*>(smem + pl.sfb_raw_off + g * kSfRawBytes),
-                           0, reinterpret_cast<uint32_t*>(smem + pl.sfb_tx_off + g * kSfTxBytes),
+        for (int a = 0; a < pl.sfb_atoms; ++a)
+          transpose_scales(reinterpret_cast<const uint32_t*>(smem + pl.sfb_raw_off + a * kSfRawBytes),
+                           0, reinterpret_cast<uint32_t*>(smem + pl.sfb_tx_off + a * kSfTxBytes),
                            lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tc_fence_after();
-          for (int g = 0; g < kG; ++g)
-            tc_cp_32x128b_warpx4(tmem + sfb_col + 4 * g,
-                                 sf_src_desc(sbase + pl.sfb_tx_off + g * kSfTxBytes));
+          for (int a = 0; a < pl.sfb_atoms; ++a)
+            tc_cp_32x128b_warpx4(tmem + kSfbCol + 4 * a,
+                                 sf_src_desc(sbase + pl.sfb_tx_off + a * kSfTxBytes));
         }
         __syncwarp();
       }
       for (int t = 0; ok && t < m.ntiles; ++t) {
-        // both sub-block slots of this tile must be free before its MMAs
-        uint32_t slot[kG];
+        const uint32_t slot = tcount & 1;
         PT_MARK();
-        for (int g = 0; g < kG; ++g) {
-          const uint32_t u = tcount * kG + g;
-          slot[g] = u % S;
-          const bool got = u < (uint32_t)S ||
-                           mbar_wait(bar_tempty(slot[g]), ((u / S) - 1) & 1, abort_flag, status, tmo);
-          if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-          }
+        const bool got = tcount < 2 ||
+                         mbar_wait(bar_tempty(slot), ((tcount >> 1) - 1) & 1, abort_flag, status, tmo);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
         PT_ADD(1);
+        TRACE(0, tcount, lane == 0);   // the tile's TMEM slot is free
         tc_fence_after();
-        const int krow = m.krow0 + t * kTileKeys;
+        const uint32_t d_tmem = tmem + slot * pl.ncols;
         for (int c = 0; c < pl.chunks; ++c) {
-          const int st = scount % nst;
           PT_MARK();
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (scount / nst) & 1, abort_flag, status, tmo))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), ph, abort_flag, status, tmo))) {
             ok = false;
             break;
           }
           PT_ADD(2);
-          if (MX) {
-            transpose_scales(
-                reinterpret_cast<const uint32_t*>(smem + pl.sfa_raw_off + st * kSfRawBytes),
-                krow & 3, reinterpret_cast<uint32_t*>(smem + pl.sfa_tx_off + st * kSfTxBytes),
-                lane);
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
+          TRACE(14, tcount, lane == 0 && c == 0);   // the tile's K stage has landed
           if (lane == 0) {
             tc_fence_after();
             const uint32_t a_base = sbase + pl.k_off + st * kStageBytes;
-            if (MX)
-              tc_cp_32x128b_warpx4(tmem + sfa_col + 4 * (tcount & 1),   // alternates per tile
+            const uint32_t b_base = sbase + pl.q_off + c * pl.qchunk;
+            if (MX)   // key scales arrive laid out for tcgen05.cp with the stage
+              tc_cp_32x128b_warpx4(tmem + kSfaCol + 4 * (tcount & 1),   // alternates per tile
                                    sf_src_desc(sbase + pl.sfa_tx_off + st * kSfTxBytes));
-            for (int g = 0; g < kG; ++g) {
-              const uint32_t b_base = sbase + pl.q_off + (g * pl.chunks + c) * pl.qchunk;
-              const uint32_t d_tmem = tmem + slot[g] * 128;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sw128_kmajor_desc(a_base, kk * 32);
-                const uint64_t bd = sw128_kmajor_desc(b_base, kk * 32);
-                const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-                if (MX)
-                  mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, pl.nsub, kk),
-                           tmem + sfa_col + 4 * (tcount & 1), tmem + sfb_col + 4 * g, acc);
-                else
-                  mma_bf16(d_tmem, ad, bd, idesc, acc);
-              }
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sw128_kmajor_desc(a_base, kk * 32);
+              const uint64_t bd = sw128_kmajor_desc(b_base, kk * 32);
+              const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
+              if (MX)
+                mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, pl.ncols, kk), tmem + kSfaCol + 4 * (tcount & 1),
+                         tmem + kSfbCol, acc);
+              else
+                mma_bf16(d_tmem, ad, bd, idesc, acc);
             }
             tc_commit(bar_empty(st));
           }
           __syncwarp();
           PT_ADD(3);
-          ++scount;
+          if (++st == (uint32_t)nst) {
+            st = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
-        if (lane == 0)
-          for (int g = 0; g < kG; ++g) tc_commit(bar_tfull(slot[g]));
+        TRACE(1, tcount, lane == 0);   // MMAs of the tile issued
+        if (lane == 0) tc_commit(bar_tfull(slot));
         __syncwarp();
         ++tcount;
       }
@@ -714,19 +758,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncwarp();
   } else {
     // ======================= epilogue warpgroups =======================
-    // kEpiWGs warpgroups; warpgroup v owns qpw consecutive queries of the item
-    // (one query at 64 heads).  Thread `row` owns key row `row` of each tile.
+    // EW warpgroups; warpgroup v owns qpw consecutive queries of the item (one
+    // query at 64 heads).  Thread `row` owns key row `row` of every tile.
     const int v = (warp - kEpiWarp0) >> 2;
     const int wq = warp & 3;                      // TMEM lane quarter = key rows wq*32..
     const int row = wq * 32 + (int)lane;          // key row of the tile owned by this thread
     const int tid = row;                          // thread index inside the warpgroup
     const int bar_id = 1 + v;
-    const int qs = pl.qs, keep = pl.keep, C = pl.cand, W = p.out_width;
-    const int qpw = qs * kG / kEpiWGs;            // queries of this warpgroup
+    const int bar_all = 1 + EW;                   // all epilogue warps
+    const int keep = pl.keep, C = pl.cand, W = p.out_width;
+    const int qpw = pl.qpw;                       // queries of this warpgroup
     const int qpw_eff = QPW_MAX == 1 ? 1 : qpw;   // compile-time when a warpgroup owns one query
     const int lq0 = v * qpw;                      // first of them, local to the item
-    const int g = lq0 / qs;                       // sub-block = TMEM slot they live in
-    const int col0 = (lq0 - g * qs) * H;          // their first accumulator column
+    const int col0 = lq0 * H;                     // their first accumulator column
     uint32_t* ckey_base = reinterpret_cast<uint32_t*>(smem + pl.cand_key_off) + lq0 * C;
     uint16_t* cidx_base = reinterpret_cast<uint16_t*>(smem + pl.cand_idx_off) + lq0 * C;
     float* w_s = reinterpret_cast<float*>(smem + pl.w_off) + lq0 * H;
@@ -779,10 +823,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
           const int t = tb + b;
           if (t < m.ntiles) {
-            const uint32_t u = tcount * kG + g;
-            const uint32_t slot = u % S;
-            ok_all &= mbar_wait(bar_tfull(slot), (u / S) & 1, abort_flag, status, tmo);
+            const uint32_t slot = tcount & 1;
+            ok_all &= mbar_wait(bar_tfull(slot), (tcount >> 1) & 1, abort_flag, status, tmo);
             PT_ADD(0);
+            TRACE(2 + v, tcount, tid == 0);   // warpgroup v woke on the tile's accumulator
             tc_fence_after();
             const int s_idx = t * kTileKeys + row;      // local key (or pool) index
             float2 part[QPW_MAX][NCH];
@@ -790,11 +834,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int qi = 0; qi < QPW_MAX; ++qi)
 #pragma unroll
               for (int c = 0; c < NCH; ++c) part[qi][c] = make_float2(0.f, 0.f);
-            // TMEM -> registers in groups of GRP columns (load, wait, reduce), to
-            // keep register pressure low; the slot goes back to the MMA warp as
-            // soon as the last group has landed.  sum_j w_j * ReLU(acc_j) with
-            // NCH independent FFMA2 chains per query.
-            const uint32_t taddr = tmem + lane_base + slot * 128 + col0;
+            // TMEM -> registers in groups of GRP columns (load, wait, reduce); the
+            // slot goes back to the MMA warp as soon as the last group has landed.
+            // sum_j w_j * ReLU(acc_j) with NCH independent FFMA2 chains per query.
+            const uint32_t taddr = tmem + lane_base + slot * pl.ncols + col0;
 #pragma unroll
             for (int gi = 0; gi < NGRP; ++gi) {
               uint32_t cb[GRP / CK][CK];
@@ -807,6 +850,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_tempty(slot));   // slot free for the MMA warp
                 PT_ADD(6);
+                TRACE(6 + v, tcount, tid == 0);   // warpgroup v released the slot
               }
 #pragma unroll
               for (int c = 0; c < GRP / CK; ++c) {
@@ -838,6 +882,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 bbal[b][qi] = __ballot_sync(0xffffffffu, vis && bkey[b][qi] > tau[qi]);
               }
             }
+            TRACE(10 + v, tcount, tid == 0);   // warpgroup v finished the tile's arithmetic
             ++tcount;
             PT_ADD(1);
           }
@@ -856,7 +901,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int b = 0; b < kBatch; ++b) {
 #pragma unroll
           for (int qi = 0; qi < QPW_MAX; ++qi) {
-            if (qi < qpw) {
+            if (qi < qpw_eff) {
               const int* cc = bcnt + (b * kMaxQpw + qi) * 4;
               const int c0 = cc[0], c1 = cc[1], c2 = cc[2], c3 = cc[3];
               const int before = (wq > 0 ? c0 : 0) + (wq > 1 ? c1 : 0) + (wq > 2 ? c2 : 0);
@@ -872,22 +917,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         PT_ADD(2);
         // ---- room for the next batch, or shrink: all warpgroups together ----
         // One vote over every epilogue thread decides, uniformly, whether to
-        // abort and whether to shrink; shrinking in lockstep lets the four
-        // queries' compactions overlap instead of stalling the shared TMEM ring
-        // one after another.
+        // abort and whether to shrink; shrinking in lockstep lets the queries'
+        // compactions overlap instead of stalling the shared TMEM ring one
+        // after another.
         bool need = false;
 #pragma unroll
         for (int qi = 0; qi < QPW_MAX; ++qi)
-          need |= qi < qpw && count[qi] + kBatch * kTileKeys > C;
-        const int vote = named_bar_or(kEpiBarAll, kEpiWGs * 128, !ok_all || *abort_flag) ? 2 : 0;
-        if (vote) {
+          need |= qi < qpw_eff && count[qi] + kBatch * kTileKeys > C;
+        if (named_bar_or(bar_all, EW * 128, !ok_all || *abort_flag)) {
           aborted = true;
           break;
         }
-        if (named_bar_or(kEpiBarAll, kEpiWGs * 128, need)) {
+        if (named_bar_or(bar_all, EW * 128, need)) {
 #pragma unroll
           for (int qi = 0; qi < QPW_MAX; ++qi) {
-            if (qi < qpw && count[qi] > keep + kTileKeys) {
+            if (qi < qpw_eff && count[qi] > keep + kTileKeys) {
               named_bar_sync(bar_id, 128);   // appends visible to the whole warpgroup
               const int cap = C - (kBatch + 2) * kTileKeys;
               int kept;
@@ -910,17 +954,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // finalize: exactly min(keep, visible) entries per query, ascending index
 #pragma unroll
       for (int qi = 0; qi < QPW_MAX; ++qi) {
-        if (qi < qpw && count[qi] > keep) {
+        if (qi < qpw_eff && count[qi] > keep) {
           int kept;
-          wg_select(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, true,
-                                    keep, wq, lane, hist, ms, bar_id, &kept);
+          wg_select(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, true, keep, wq, lane, hist,
+                    ms, bar_id, &kept);
           count[qi] = kept;
         }
       }
 #pragma unroll
       for (int qi = 0; qi < QPW_MAX; ++qi) {
         const int tq = qbase + qi;
-        if (qi >= qpw || tq >= m.L) continue;
+        if (qi >= qpw_eff || tq >= m.L) continue;
         const size_t orow = (size_t)(a + tq) * W;
         const int n = count[qi];
         const uint32_t* ck = ckey_base + qi * C;
@@ -1066,10 +1110,20 @@ __global__ void __launch_bounds__(128, 1) debug_mma_tile_kernel(const __grid_con
 // launchers (called from api.cu)
 // ----------------------------------------------------------------------------
 cudaError_t launch_build_worklist(const int32_t* cu, int num_seqs, int total_tokens, int max_seqlen,
-                                  int tq, int pool, int2* items, int* doc_prefix, int* hdr,
-                                  int max_items, cudaStream_t stream) {
+                                  int tq, int pool, int2* items, int* doc_prefix, int* tile_base,
+                                  int* hdr, int max_items, cudaStream_t stream) {
   build_worklist_kernel<<<1, kWLThreads, 0, stream>>>(cu, num_seqs, total_tokens, max_seqlen, tq,
-                                                      pool, items, doc_prefix, hdr, max_items);
+                                                      pool, items, doc_prefix, tile_base, hdr, max_items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const int32_t* cu_keys,
+                                 const int* tile_base, int num_seqs, int max_tiles, uint32_t* out,
+                                 int sm_count, cudaStream_t stream) {
+  int grid = max_tiles < sm_count * 8 ? max_tiles : sm_count * 8;
+  if (grid < 1) grid = 1;
+  build_tiled_kscales_kernel<<<grid, 128, 0, stream>>>(reinterpret_cast<const uint32_t*>(k_scale), k_rows,
+                                                       cu_keys, tile_base, num_seqs, max_tiles, out);
   return cudaGetLastError();
 }
 
@@ -1078,7 +1132,7 @@ static cudaError_t launch_score_t(const ScoreParams& p, int grid, cudaStream_t s
   auto kern = score_topk_kernel<PREC, H>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.total);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kScoreThreads, p.plan.total, stream>>>(p);
+  kern<<<grid, score_threads(PREC), p.plan.total, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1127,6 +1181,12 @@ extern "C" void dsa_idx_debug_phase_timers(unsigned long long* out64, int reset)
     unsigned long long z[64] = {0};
     cudaMemcpyToSymbol(g_phase_cycles, z, sizeof(z));
   }
+}
+#endif
+
+#ifdef DSA_TRACE
+extern "C" void dsa_idx_debug_trace(long long* out) {
+  cudaMemcpyFromSymbol(out, g_trace, sizeof(long long) * 16 * 256);
 }
 #endif
 
