@@ -324,6 +324,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Barrier over `nthreads` threads that also counts the threads whose
+// predicate is true.
+__device__ __forceinline__ int named_bar_popc(int id, int nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return (int)out;
+}
+
 // Barrier over `nthreads` threads that also ORs a predicate across them.
 __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
   uint32_t out;

@@ -22,7 +22,7 @@ constexpr int kMiscInts = 320;       // per-warpgroup scratch ints
 constexpr int kBatch = 4;            // key tiles scored between two appends
 constexpr int kMaxQpw = 4;           // queries per epilogue warpgroup (at most)
 constexpr int kMaxStages = 6;
-constexpr int kMaxCand = 4096;
+constexpr int kMaxCand = 8192;      // candidate entries per query (at most)
 constexpr int kSfaCol = 384;         // MXFP8: key scales, 2 x 4 TMEM columns (alternating per tile)
 constexpr int kSfbCol = 392;         // MXFP8: query scales, up to 2 atoms x 4 columns
 
@@ -82,7 +82,49 @@ struct ScoreParams {
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// Host-side planner: returns false when no configuration fits.
+// K-tile stages the planner keeps before it grows the candidate buffers: two
+// key tiles in flight behind the one being multiplied (a BF16 tile at
+// head_dim 128 is two 128-byte chunks, so two stages).
+inline int min_stages(int prec, int chunks) { return prec == PREC_BF16 ? 2 * chunks : 4; }
+
+// Lays out shared memory for (qpw, cand, nst); returns the total bytes.
+inline int layout_score_plan(ScorePlan* s, int nst) {
+  const bool sf = s->prec == PREC_MXFP8;
+  int off = 0;
+  s->q_off = off;
+  off += s->chunks * s->qchunk;
+  s->k_off = off;
+  s->nst = nst;
+  off += nst * kStageBytes;
+  s->sfa_raw_off = off;   // unused: key scales arrive already laid out for tcgen05.cp
+  s->sfa_tx_off = off;
+  off += sf ? nst * kSfTxBytes : 0;
+  s->sfb_raw_off = off;
+  off += sf ? 2 * kSfRawBytes : 0;
+  s->sfb_tx_off = off;
+  off += sf ? 2 * kSfTxBytes : 0;
+  s->cand_key_off = off;
+  off += s->nq * s->cand * 4;
+  s->cand_idx_off = off;
+  off += s->nq * s->cand * 2;
+  off = round_up(off, 16);
+  s->w_off = off;
+  off += s->nq * s->n_heads * 4;
+  s->hist_off = off;
+  off += s->ewgs * 256 * 4;
+  s->misc_off = off;
+  off += s->ewgs * kMiscInts * 4;
+  off = round_up(off, 8);
+  s->bar_off = off;
+  off += 512;
+  s->total = off + 1024;   // slack for aligning the dynamic smem base to 1024
+  return s->total;
+}
+
+// Host-side planner: returns false when no configuration fits.  Shared memory
+// goes first to min_stages() K stages, then to the candidate buffers (fewer
+// shrinks; at most 4 * keep, and kMaxCand, entries per query), then to more
+// stages.
 inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, ScorePlan* p) {
   ScorePlan s{};
   s.prec = prec;
@@ -93,68 +135,35 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
   const int elem = prec == PREC_BF16 ? 2 : 1;
   const bool sf = prec == PREC_MXFP8;
   s.chunks = head_dim * elem / kChunkBytes;
-  const int cand_min = keep + (kBatch + 2) * kTileKeys;   // a full batch fits after a shrink
-  int qpw = qpw_max(prec, n_heads);
-  int cand = round_up(keep * 2 > cand_min ? keep * 2 : cand_min, 128);
-  if (cand > kMaxCand) cand = round_up(cand_min, 128);
-  if (cand > kMaxCand || qpw < 1) return false;
-  for (;;) {
+  const int cand_min = round_up(keep + (kBatch + 2) * kTileKeys, 128);   // a full batch fits after a shrink
+  if (cand_min > kMaxCand) return false;
+  const int cand_cap = 4 * keep > cand_min ? (4 * keep < kMaxCand ? round_up(4 * keep, 128) : kMaxCand) : cand_min;
+  for (int qpw = qpw_max(prec, n_heads); qpw >= 1; qpw /= 2) {
     s.qpw = qpw;
     s.nq = s.ewgs * qpw;
     s.ncols = s.nq * n_heads;
     if (s.ncols < 16 || s.ncols % 16 != 0 || s.ncols > max_ncols(prec)) return false;
-    s.cand = cand;
     s.qchunk = s.ncols * kChunkBytes;   // multiple of 1024: keeps the swizzle atoms aligned
     s.sfb_atoms = sf ? (s.ncols + 127) / 128 : 0;
-    int off = 0;
-    s.q_off = off;
-    off += s.chunks * s.qchunk;
-    s.k_off = off;
-    const int rest = s.nq * cand * 6 + s.nq * n_heads * 4 + s.ewgs * 256 * 4 + s.ewgs * kMiscInts * 4 + 512 + 64;
-    const int per_stage = kStageBytes + (sf ? kSfTxBytes : 0);
-    const int sfb = sf ? 2 * (kSfRawBytes + kSfTxBytes) : 0;
-    int nst = (kMaxSmem - 1024 - off - rest - sfb) / per_stage;
-    if (nst > kMaxStages) nst = kMaxStages;
-    if (nst >= 2) {
-      s.nst = nst;
-      off += nst * kStageBytes;
-      s.sfa_raw_off = off;   // unused: key scales arrive already laid out for tcgen05.cp
-      s.sfa_tx_off = off;
-      off += sf ? nst * kSfTxBytes : 0;
-      s.sfb_raw_off = off;
-      off += sf ? 2 * kSfRawBytes : 0;
-      s.sfb_tx_off = off;
-      off += sf ? 2 * kSfTxBytes : 0;
-      s.cand_key_off = off;
-      off += s.nq * cand * 4;
-      s.cand_idx_off = off;
-      off += s.nq * cand * 2;
-      off = round_up(off, 16);
-      s.w_off = off;
-      off += s.nq * n_heads * 4;
-      s.hist_off = off;
-      off += s.ewgs * 256 * 4;
-      s.misc_off = off;
-      off += s.ewgs * kMiscInts * 4;
-      off = round_up(off, 8);
-      s.bar_off = off;
-      off += 512;
-      s.total = off + 1024;   // slack for aligning the dynamic smem base to 1024
+    for (int nmin = min_stages(prec, s.chunks); nmin >= 2; --nmin) {
+      // the largest buffer that fits beside nmin stages
+      s.cand = 0;
+      const int base = layout_score_plan(&s, nmin);
+      int cand = (kMaxSmem - base) / (s.nq * 6) / 128 * 128;
+      if (cand > cand_cap) cand = cand_cap;
+      for (; cand >= cand_min; cand -= 128) {
+        s.cand = cand;
+        if (layout_score_plan(&s, nmin) <= kMaxSmem) break;
+      }
+      if (cand < cand_min) continue;
+      int nst = nmin;   // spare bytes become more stages
+      while (nst < kMaxStages && layout_score_plan(&s, nst + 1) <= kMaxSmem) ++nst;
+      layout_score_plan(&s, nst);
       *p = s;
-      return s.total <= kMaxSmem;
+      return true;
     }
-    if (cand > round_up(cand_min, 128)) {
-      cand = round_up(cand_min, 128);
-      continue;
-    }
-    if (qpw > 1) {
-      qpw /= 2;
-      cand = round_up(keep * 2 > cand_min ? keep * 2 : cand_min, 128);
-      if (cand > kMaxCand) cand = round_up(cand_min, 128);
-      continue;
-    }
-    return false;
   }
+  return false;
 }
 
 }  // namespace dsa

@@ -281,8 +281,8 @@ enum {
   MS_MAX = 20,          // [4]
   MS_RCNT = 24,         // [2][8] per-warp counts of a compaction round
   MS_BCNT = 48,         // [2][kBatch][kMaxQpw][4] per-warp append counts of a batch
-  MS_CAND = 176,
-  MS_CNT4 = 180,        // [4]
+  MS_CAND = 176,        // [2] the two sampled thresholds
+  MS_CNT4 = 180,        // [2][4] per-warp counts above the two sampled thresholds
   MS_SORT = 192,        // [128] sample keys (sort exchange)
 };
 
@@ -468,18 +468,44 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
       sk = (low == desc) ? max(sk, other) : min(sk, other);
     }
   }
-  int r = (int)((((long long)keep + cap_after) / 2 * 128) / n);
-  r = r < 0 ? 0 : (r > 127 ? 127 : r);
-  if (tid == r) ms[MS_CAND] = (int)sk;
+  // Two thresholds from the sorted samples (descending: sample r has about
+  // (r + 1) * n / 128 entries at or above it): a tight one aimed at keep + 1
+  // sigma entries and a safe one at keep + 3 sigma, where sigma = n *
+  // sqrt(f (1 - f) / 128), f = keep / n, is the spread of that count.  One
+  // pass counts both; the tight one wins whenever it keeps enough.
+  const float nf = (float)n, f = (float)keep / nf;
+  const float sig = nf * sqrtf(f * (1.f - f) * (1.f / 128.f));
+  int ra = (int)ceilf(((float)keep + sig) * 128.f / nf) - 1;
+  int rs = (int)ceilf(((float)keep + 3.f * sig) * 128.f / nf) - 1;
+  ra = ra < 0 ? 0 : (ra > 127 ? 127 : ra);
+  rs = rs < 0 ? 0 : (rs > 127 ? 127 : rs);
+  if (tid == ra) ms[MS_CAND] = (int)sk;
+  if (tid == rs) ms[MS_CAND + 1] = (int)sk;
   named_bar_sync(bar_id, 128);
-  const uint32_t cand = (uint32_t)ms[MS_CAND];
-  int c = 0;
-  for (int e = tid; e < n; e += 128) c += keys[e] >= cand ? 1 : 0;
-  c = __reduce_add_sync(0xffffffffu, c);
-  if (lane == 0) ms[MS_CNT4 + wq] = c;
+  const uint32_t cand_a = (uint32_t)ms[MS_CAND], cand_s = (uint32_t)ms[MS_CAND + 1];
+  int ca = 0, cs = 0;
+  for (int e = tid; e < n; e += 128) {
+    const uint32_t kv = keys[e];
+    ca += kv >= cand_a ? 1 : 0;
+    cs += kv >= cand_s ? 1 : 0;
+  }
+  ca = __reduce_add_sync(0xffffffffu, ca);
+  cs = __reduce_add_sync(0xffffffffu, cs);
+  if (lane == 0) {
+    ms[MS_CNT4 + wq] = ca;
+    ms[MS_CNT4 + 4 + wq] = cs;
+  }
   named_bar_sync(bar_id, 128);
-  const int total = ms[MS_CNT4 + 0] + ms[MS_CNT4 + 1] + ms[MS_CNT4 + 2] + ms[MS_CNT4 + 3];
-  if (total < keep || total > cap_after) return false;   // uniform: every thread read the same counts
+  // uniform: every thread reads the same counts
+  const int tot_a = ms[MS_CNT4 + 0] + ms[MS_CNT4 + 1] + ms[MS_CNT4 + 2] + ms[MS_CNT4 + 3];
+  const int tot_s = ms[MS_CNT4 + 4] + ms[MS_CNT4 + 5] + ms[MS_CNT4 + 6] + ms[MS_CNT4 + 7];
+  uint32_t cand;
+  if (tot_a >= keep && tot_a <= cap_after)
+    cand = cand_a;
+  else if (tot_s >= keep && tot_s <= cap_after)
+    cand = cand_s;
+  else
+    return false;
   // stable compaction in rounds of 512 entries
   const uint32_t lt = (1u << lane) - 1u;
   int out = 0;
@@ -592,7 +618,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
     // ======================= TMA producer =======================
     if (lane == 0) {
       PT_DECL
-      uint32_t scount = 0, st = 0, ph = 0;
+      uint32_t scount = 0, st = 0, ph = 0, ptile = 0;
       bool wrapped = false;
       int it = 0;
       bool ok = true;
@@ -627,6 +653,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             }
             PT_ADD(1);
             if (!(p.fault_inject == 1 && scount == 0)) {   // test hook: stage 0 is never loaded
+              TRACE(15, ptile, c == 0);   // producer issues the tile's first K stage
               mbar_arrive_expect_tx(bar_full(st), k_bytes);
               tma_load_2d(sbase + pl.k_off + st * kStageBytes, &p.tm_k, bar_full(st),
                           c * chunk_elems, krow);
@@ -642,6 +669,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               wrapped = true;
             }
           }
+          ++ptile;
         }
       }
       // drain: every load this thread issued has landed before the CTA exits
@@ -665,6 +693,12 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
     int it = 0;
     bool ok = true;
     const uint32_t idesc = MX ? 0u : idesc_bf16(128, pl.ncols);
+    uint32_t idesc_k[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) idesc_k[kk] = idesc_mxf8(128, pl.ncols, kk);
+    const uint64_t a_desc0 = sw128_kmajor_desc(sbase + pl.k_off, 0);    // stage 0, K step 0
+    const uint64_t b_desc0 = sw128_kmajor_desc(sbase + pl.q_off, 0);    // chunk 0, K step 0
+    const uint64_t sf_desc0 = sf_src_desc(sbase + pl.sfa_tx_off);       // stage 0 key scales
     for (int r = 0; ok && r * G < nitems; ++r) {
       const int i = item_index(r, nitems);
       if (i < 0) continue;
@@ -714,21 +748,19 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
           TRACE(14, tcount, lane == 0 && c == 0);   // the tile's K stage has landed
           if (lane == 0) {
             tc_fence_after();
-            const uint32_t a_base = sbase + pl.k_off + st * kStageBytes;
-            const uint32_t b_base = sbase + pl.q_off + c * pl.qchunk;
+            // descriptors: start address field + 2 per 32-byte K step
+            const uint64_t ad0 = a_desc0 + (uint64_t)(st * (kStageBytes >> 4));
+            const uint64_t bd0 = b_desc0 + (uint64_t)(c * (pl.qchunk >> 4));
+            const uint32_t sfa = tmem + kSfaCol + 4 * (tcount & 1);   // alternates per tile
             if (MX)   // key scales arrive laid out for tcgen05.cp with the stage
-              tc_cp_32x128b_warpx4(tmem + kSfaCol + 4 * (tcount & 1),   // alternates per tile
-                                   sf_src_desc(sbase + pl.sfa_tx_off + st * kSfTxBytes));
+              tc_cp_32x128b_warpx4(sfa, sf_desc0 + (uint64_t)(st * (kSfTxBytes >> 4)));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sw128_kmajor_desc(a_base, kk * 32);
-              const uint64_t bd = sw128_kmajor_desc(b_base, kk * 32);
               const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
               if (MX)
-                mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, pl.ncols, kk), tmem + kSfaCol + 4 * (tcount & 1),
-                         tmem + kSfbCol, acc);
+                mma_mxf8(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc_k[kk], sfa, tmem + kSfbCol, acc);
               else
-                mma_bf16(d_tmem, ad, bd, idesc, acc);
+                mma_bf16(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
             }
             tc_commit(bar_empty(st));
           }
@@ -897,38 +929,48 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         }
         ++nbatch;
         named_bar_sync(bar_id, 128);      // batch counts of this warpgroup visible
+        TRACE(5, nbatch, tid == 0 && v == 0 && EW < 4);   // batch counts exchanged
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
+        for (int qi = 0; qi < QPW_MAX; ++qi) {
+          if (qi < qpw_eff) {
+            // the query's counts for the whole batch first: no load waits behind an append
+            int4 cc[kBatch];
 #pragma unroll
-          for (int qi = 0; qi < QPW_MAX; ++qi) {
-            if (qi < qpw_eff) {
-              const int* cc = bcnt + (b * kMaxQpw + qi) * 4;
-              const int c0 = cc[0], c1 = cc[1], c2 = cc[2], c3 = cc[3];
-              const int before = (wq > 0 ? c0 : 0) + (wq > 1 ? c1 : 0) + (wq > 2 ? c2 : 0);
+            for (int b = 0; b < kBatch; ++b) cc[b] = *reinterpret_cast<const int4*>(bcnt + (b * kMaxQpw + qi) * 4);
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+              const int before = (wq > 0 ? cc[b].x : 0) + (wq > 1 ? cc[b].y : 0) + (wq > 2 ? cc[b].z : 0);
               if ((bbal[b][qi] >> lane) & 1u) {
                 const int pos = count[qi] + before + __popc(bbal[b][qi] & lt);
                 ckey_base[qi * C + pos] = bkey[b][qi];
                 cidx_base[qi * C + pos] = (uint16_t)((tb + b) * kTileKeys + row);
               }
-              count[qi] += c0 + c1 + c2 + c3;
+              count[qi] += cc[b].x + cc[b].y + cc[b].z + cc[b].w;
             }
           }
         }
         PT_ADD(2);
+        TRACE(9, nbatch, tid == 0 && v == 0 && EW < 4);   // batch appended
         // ---- room for the next batch, or shrink: all warpgroups together ----
         // One vote over every epilogue thread decides, uniformly, whether to
         // abort and whether to shrink; shrinking in lockstep lets the queries'
         // compactions overlap instead of stalling the shared TMEM ring one
-        // after another.
+        // after another.  One barrier carries both votes: lane 0 of each warp
+        // reports an abort, lanes 1..31 a shrink, so the count it returns is
+        // (warps aborting) + 31 * (warps needing room), with at most 16 warps.
         bool need = false;
 #pragma unroll
         for (int qi = 0; qi < QPW_MAX; ++qi)
           need |= qi < qpw_eff && count[qi] + kBatch * kTileKeys > C;
-        if (named_bar_or(bar_all, EW * 128, !ok_all || *abort_flag)) {
+        need = __any_sync(0xffffffffu, need);
+        const bool warp_abort = __any_sync(0xffffffffu, !ok_all || *abort_flag);
+        const int votes = named_bar_popc(bar_all, EW * 128, lane == 0 ? warp_abort : need);
+        if (votes % 31 != 0) {
           aborted = true;
           break;
         }
-        if (named_bar_or(bar_all, EW * 128, need)) {
+        TRACE(13, nbatch, tid == 0 && v == 0 && EW < 4);   // vote taken
+        if (votes != 0) {
 #pragma unroll
           for (int qi = 0; qi < QPW_MAX; ++qi) {
             if (qi < qpw_eff && count[qi] > keep + kTileKeys) {
