@@ -175,14 +175,15 @@ dsa_status_t dsa_idx_kpool_compress(
  *   k_scale  device u8 [rows of k, head_dim/32] (MXFP8), else NULL
  *   w        device [total_tokens, n_heads], w_dtype (FP32 or BF16)
  *   sm_scale scalar multiplier of the score
- *   index_topk  keys selected per query (pool mode: multiple of kpool_size;
- *               kpool_size*... pools = index_topk / kpool_size)
+ *   index_topk  keys selected per query; in pool mode a multiple of
+ *               kpool_size, and index_topk / kpool_size pools are kept
  *   prec     BF16 (kind::f16) or MXFP8 (block-scaled kind::mxf8f6f4)
  *   flags    DSA_FLAG_* bits
  *   kpool_size  1 = plain keys; >1 = pool mode (cu_pools required)
  *   topk_idx    device int32 [total_tokens, W] (W = dsa_idx_output_width):
- *               selected local indices, ascending (or by score with
- *               DSA_FLAG_SORT_BY_SCORE), then -1 padding.  Pool mode: the
+ *               selected local indices in ascending order, then -1
+ *               padding (DSA_FLAG_SORT_BY_SCORE is reserved and returns
+ *               DSA_ERR_UNSUPPORTED).  Pool mode: the
  *               expanded tokens of the selected pools, then the tail tokens.
  *   topk_score  device fp32 [total_tokens, W] or NULL: the score of each
  *               entry (pooled score for pool tokens, +INF for tail tokens,
@@ -191,7 +192,9 @@ dsa_status_t dsa_idx_kpool_compress(
  *   ws, ws_bytes  device workspace of dsa_idx_workspace_size() bytes
  * Ties are broken towards the lower index; -0 and +0 compare equal.
  * Supported: head_dim 128 (BF16 also 64), n_heads in {4,8,16,32,64},
- * 1 <= index_topk <= 2048, max_seqlen <= 65536. */
+ * 1 <= index_topk <= 2048 (MXFP8 with 4 heads: <= 1664, the candidate
+ * buffers of its 12 queries per block must fit in shared memory),
+ * max_seqlen <= 65536.  Other shapes return DSA_ERR_UNSUPPORTED. */
 dsa_status_t dsa_idx_score_topk(
     const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
     const void* w, dsa_dtype_t w_dtype, float sm_scale,

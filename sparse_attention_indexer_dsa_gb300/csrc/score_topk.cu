@@ -437,11 +437,12 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
 }
 
 // Approximate shrink from a sample: sort 128 evenly spaced entries
-// (bitonic, descending), take the sample key at the rank that maps to the
-// middle of [keep, cap_after], count the entries >= it exactly, and if that
-// count lies in the window keep exactly those entries (stable, in place).
-// Returns false and changes nothing when the count misses the window (heavy
-// ties, skewed samples); the caller then uses the radix select.  On success
+// (bitonic, descending), take two sample keys as candidate thresholds (see
+// below), count the entries >= each exactly in one pass, and keep exactly the
+// entries >= the tighter threshold whose count lies in [keep, cap_after]
+// (stable, in place).  Returns false and changes nothing when neither count
+// lies in the window (heavy ties, skewed samples); the caller then uses the
+// radix select.  On success
 // *tau_out is the new acceptance threshold (candidate - 1: later keys equal to
 // it are still accepted, so nothing that may belong to the top-k is lost).
 __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, int n, int keep,
