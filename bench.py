@@ -155,6 +155,100 @@ def oracle_sample_rate(wl, x, n_rows, seed=0):
     return n_rows / dt, dt, rows
 
 
+def oracle_rate(wl, x, prec, n_rows, seed=0):
+    """Queries/s of the CPU oracle on `n_rows` query rows of any workload
+    (uniformly spread positions), including the key-side work those rows
+    need (LayerNorm/RoPE/quantisation, or KPool compression)."""
+    import oracle.dsa_oracle as O
+    rng = np.random.default_rng(seed)
+    T, H, D = wl.total_tokens, wl.n_heads, wl.head_dim
+    rows = np.sort(rng.choice(T, size=min(n_rows, T), replace=False))
+    cu = wl.cu_seqlens
+    t0 = time.perf_counter()
+    pos = O.positions_in_document(cu)
+    kk = x["k"].astype(np.float64)
+    qr = x["q"][rows].astype(np.float64)
+    if wl.layernorm:
+        kk = O.key_layernorm(x["k"], x["ln_gamma"], x["ln_beta"], 1e-6)
+    if wl.rope_dim:
+        kk = O.round_fp32(O.apply_rope(kk, pos, wl.rope_dim, wl.rope_base))
+        qr = O.round_fp32(O.apply_rope(qr, pos[rows][:, None], wl.rope_dim, wl.rope_base))
+    qq = np.zeros((T, H, D))
+    w = x["w"].astype(np.float64)
+    if wl.kpool > 1:
+        kbar, cpools = O.kpool_compress(x["k"], O.bf16_bits_to_float(x["gate_bits"]), x["slot_bias"], cu, wl.kpool)
+        qq[rows] = O.round_bf16(qr)
+        O.kpool_topk(qq, O.round_bf16(kbar), w, cu, cpools, wl.index_topk, wl.kpool, True, rows=rows)
+    else:
+        kq = O.scoring_operand(kk, prec)[0]
+        qq[rows] = O.scoring_operand(qr.reshape(-1, D), prec)[0].reshape(len(rows), H, D)
+        O.indexer_topk(qq, kq, w, cu, wl.index_topk, rows=rows)
+    dt = time.perf_counter() - t0
+    return len(rows) / dt, dt
+
+
+def run_table(args):
+    """Every configuration x precision: GPU score + top-k time (CUDA events,
+    median of 5 after 2 warm-ups, L2 flushed before each), queries/s,
+    TFLOP/s, % of peak, and the oracle's queries/s on a row sample.  Prints
+    a markdown table (not the JSON line)."""
+    import torch
+    import sparse_attention_indexer_dsa_gb300 as dsa
+
+    torch.cuda.set_device(0)
+    devn = torch.device("cuda", 0)
+    peaks, peak_kind = load_peaks()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=devn)
+    cases = [("tiny", "bf16"), ("c2", "bf16"), ("c3", "mxfp8"), ("c3", "bf16"), ("thd", "mxfp8"),
+             ("kpool", "bf16"), ("target", "mxfp8"), ("target", "bf16")]
+    print(f"| config | precision | score+top-k ms | queries/s | TFLOP/s | % of {peak_kind} peak | "
+          f"oracle queries/s ({os.cpu_count()} cores, rows) |")
+    print("|---|---|---:|---:|---:|---:|---:|")
+    for name, prec in cases:
+        wl = W.config(name)
+        x = W.make_inputs(wl)
+        T, H, D, K = wl.total_tokens, wl.n_heads, wl.head_dim, wl.index_topk
+        cu = torch.from_numpy(wl.cu_seqlens).to(devn)
+        q = torch.from_numpy(x["q"]).to(devn)
+        k = torch.from_numpy(x["k"]).to(devn)
+        w = torch.from_numpy(x["w"]).to(devn)
+        g = torch.from_numpy(x["ln_gamma"]).to(devn) if wl.layernorm else None
+        b = torch.from_numpy(x["ln_beta"]).to(devn) if wl.layernorm else None
+        qo, qs, ko, ks = dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False,
+                                        True, prec)
+        pool = {}
+        if wl.kpool > 1:
+            gate = torch.from_numpy(x["gate_bits"].view(np.int16)).to(devn)
+            ko, cpools = dsa.kpool_compress(k, gate, torch.from_numpy(x["slot_bias"]).to(devn), cu, wl.kpool)
+            ks = None
+            pool = dict(kpool_size=wl.kpool, cu_pools=cpools, tail=True)
+        ws = dsa.workspace(T, len(wl.doc_lens), wl.max_seqlen, H, D, K, wl.kpool, prec, devn)
+
+        def run():
+            return dsa.score_topk(qo, qs, ko, ks, w, cu, wl.max_seqlen, H, K, prec, ws=ws, **pool)
+
+        for _ in range(2):
+            run()
+        ts = []
+        for r in range(5):
+            flush.fill_(r)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        if dsa.read_status(ws) != 0:
+            raise RuntimeError(f"{name} {prec}: device status {dsa.read_status(ws)}")
+        ms = statistics.median(ts)
+        tf = wl.flops() / ms / 1e9
+        peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if prec == "mxfp8" else 1.0)
+        n_rows = min(T, args.ref_rows // 8 if T > 4096 else 64)
+        orate, _ = oracle_rate(wl, x, prec, n_rows)
+        print(f"| {describe(wl)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
+              f"{100 * tf / peak:.1f} | {orate:,.1f} ({n_rows}) |", flush=True)
+
+
 def run_reference(args, wl):
     world, rank, _ = dist_setup(args.gpus)
     if rank != 0:
@@ -204,8 +298,8 @@ def run_native(args, wl):
     q = torch.from_numpy(x["q"]).to(devn)
     k = torch.from_numpy(x["k"]).to(devn)
     w = torch.from_numpy(x["w"]).to(devn)
-    g = torch.from_numpy(x["ln_gamma"]).to(devn)
-    b = torch.from_numpy(x["ln_beta"]).to(devn)
+    g = torch.from_numpy(x["ln_gamma"]).to(devn) if wl.layernorm else None
+    b = torch.from_numpy(x["ln_beta"]).to(devn) if wl.layernorm else None
     cu = torch.from_numpy(cu_np).to(devn)
     prec = wl.prec
     ws = dsa.workspace(T, len(wl.doc_lens), wl.max_seqlen, H, D, K, 1, prec, devn)
@@ -371,9 +465,13 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=3072)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--table", action="store_true",
+                    help="time every configuration and print a markdown table instead of the JSON line")
     args = ap.parse_args()
     wl = W.config(args.workload)
-    if args.impl == "reference":
+    if args.table:
+        run_table(args)
+    elif args.impl == "reference":
         run_reference(args, wl)
     else:
         run_native(args, wl)

@@ -562,6 +562,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
   constexpr int GRP = (score_threads(PREC) <= 448 || NCOLW < 32) ? NCOLW : 32;   // columns per load/wait group
   constexpr int NGRP = NCOLW / GRP;
   constexpr int NCH = (H / 4) < 4 ? (H / 4) : 4;     // independent FFMA2 chains per query
+  constexpr bool FRAG = QPW_MAX == 1 && H == 64;      // one query of 64 heads per warpgroup
   static_assert(QPW_MAX >= 1 && QPW_MAX <= kMaxQpw, "queries per warpgroup");
   const ScorePlan& pl = p.plan;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -841,6 +842,12 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         vis_lim[qi] = tq >= m.L ? -1 : (p.pool > 1 ? (tq + 1) / p.pool - 1 : tq);
       }
       named_bar_sync(bar_id, 128);
+      // fragment path: this thread's 16 head weights stay in registers for the item
+      float2 wp[FRAG ? 8 : 1];
+      if constexpr (FRAG) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wp[i] = *reinterpret_cast<const float2*>(w_s + 8 * i + 2 * (lane & 3));
+      }
       PT_ADD(5);
       for (int tb = 0; tb < m.ntiles; tb += kBatch) {
         // ---- score kBatch tiles; keep keys and ballots in registers ----
@@ -862,57 +869,120 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             TRACE(2 + v, tcount, tid == 0);   // warpgroup v woke on the tile's accumulator
             tc_fence_after();
             const int s_idx = t * kTileKeys + row;      // local key (or pool) index
-            float2 part[QPW_MAX][NCH];
+            if constexpr (FRAG) {
+              // Fragment layout (.16x256b): thread t holds 16 heads (2(t%4) + 8i, +1) of
+              // the four key rows g, g+8, g+16, g+24 (g = t/4) of its warp's 32 rows, so
+              // its head weights fit in registers.  Row sums are then reduced over the
+              // four threads of a row group and moved to lane = row.
+              const uint32_t tcol = tmem + lane_base + slot * pl.ncols + col0;
+              float2 acc[4];
 #pragma unroll
-            for (int qi = 0; qi < QPW_MAX; ++qi)
+              for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.f, 0.f);
+              auto frag_sum = [&](const uint32_t* f, float2& a0, float2& a1) {
 #pragma unroll
-              for (int c = 0; c < NCH; ++c) part[qi][c] = make_float2(0.f, 0.f);
-            // TMEM -> registers in groups of GRP columns (load, wait, reduce); the
-            // slot goes back to the MMA warp as soon as the last group has landed.
-            // sum_j w_j * ReLU(acc_j) with NCH independent FFMA2 chains per query.
-            const uint32_t taddr = tmem + lane_base + slot * pl.ncols + col0;
-#pragma unroll
-            for (int gi = 0; gi < NGRP; ++gi) {
-              uint32_t cb[GRP / CK][CK];
-#pragma unroll
-              for (int c = 0; c < GRP / CK; ++c) tmem_load_cols<CK>(taddr + gi * GRP + c * CK, cb[c]);
-#pragma unroll
-              for (int c = 0; c < GRP / CK; ++c) tmem_wait_tied<CK>(cb[c]);
-              if (gi == NGRP - 1) {
+                for (int i = 0; i < 8; ++i) {
+                  a0 = ffma2(wp[i], make_float2(fmaxf(__uint_as_float(f[4 * i]), 0.f),
+                                                fmaxf(__uint_as_float(f[4 * i + 1]), 0.f)), a0);
+                  a1 = ffma2(wp[i], make_float2(fmaxf(__uint_as_float(f[4 * i + 2]), 0.f),
+                                                fmaxf(__uint_as_float(f[4 * i + 3]), 0.f)), a1);
+                }
+              };
+              auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_tempty(slot));   // slot free for the MMA warp
                 PT_ADD(6);
                 TRACE(6 + v, tcount, tid == 0);   // warpgroup v released the slot
+              };
+              uint32_t fa[32];
+              if constexpr (GRP == 64) {   // both 16-lane halves in flight at once
+                uint32_t fb[32];
+                tmem_ld_16x256b_x8(tcol, fa);
+                tmem_ld_16x256b_x8(tcol + (16u << 16), fb);
+                tmem_wait_tied<16>(fa);
+                tmem_wait_tied<16>(fa + 16);
+                tmem_wait_tied<16>(fb);
+                tmem_wait_tied<16>(fb + 16);
+                release();
+                frag_sum(fa, acc[0], acc[1]);
+                frag_sum(fb, acc[2], acc[3]);
+              } else {                      // one half at a time (fewer registers)
+                tmem_ld_16x256b_x8(tcol, fa);
+                tmem_wait_tied<16>(fa);
+                tmem_wait_tied<16>(fa + 16);
+                frag_sum(fa, acc[0], acc[1]);
+                tmem_ld_16x256b_x8(tcol + (16u << 16), fa);
+                tmem_wait_tied<16>(fa);
+                tmem_wait_tied<16>(fa + 16);
+                release();
+                frag_sum(fa, acc[2], acc[3]);
               }
-#pragma unroll
-              for (int c = 0; c < GRP / CK; ++c) {
-#pragma unroll
-                for (int j4 = 0; j4 < CK / 4; ++j4) {
-                  const int col = gi * GRP + c * CK + 4 * j4;
-                  const int qi = col / H, hh = col % H;
-                  if (qi < qpw_eff) {
-                    const float4 wv = *reinterpret_cast<const float4*>(w_s + qi * H + hh);
-                    const uint32_t* x = cb[c] + 4 * j4;
-                    const float2 r0 = make_float2(fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
-                    const float2 r1 = make_float2(fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
-                    float2& pc = part[qi][(hh / 4) % NCH];
-                    pc = ffma2(make_float2(wv.x, wv.y), r0, pc);
-                    pc = ffma2(make_float2(wv.z, wv.w), r1, pc);
+              // reduce-scatter over the 4 lanes of a row group: lane t ends with the
+              // total of row g + 8 (t % 4)
+              const float s0 = acc[0].x + acc[0].y, s1 = acc[1].x + acc[1].y;
+              const float s2 = acc[2].x + acc[2].y, s3 = acc[3].x + acc[3].y;
+              const bool b1 = (lane >> 1) & 1u, b0 = lane & 1u;
+              const float k0 = (b1 ? s2 : s0) + __shfl_xor_sync(0xffffffffu, b1 ? s0 : s2, 2);
+              const float k1 = (b1 ? s3 : s1) + __shfl_xor_sync(0xffffffffu, b1 ? s1 : s3, 2);
+              const float own = (b0 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b0 ? k0 : k1, 1);
+              // row r's total sits in lane 4 (r % 8) + r / 8
+              const float sv = __shfl_sync(0xffffffffu, own, 4 * (lane & 7u) + (lane >> 3)) * p.sm_scale;
+              const bool vis = s_idx <= vis_lim[0];
+              bkey[b][0] = orderable_key(sv);
+              bbal[b][0] = __ballot_sync(0xffffffffu, vis && bkey[b][0] > tau[0]);
+            } else {
+              float2 part[QPW_MAX][NCH];
+  #pragma unroll
+              for (int qi = 0; qi < QPW_MAX; ++qi)
+  #pragma unroll
+                for (int c = 0; c < NCH; ++c) part[qi][c] = make_float2(0.f, 0.f);
+              // TMEM -> registers in groups of GRP columns (load, wait, reduce); the
+              // slot goes back to the MMA warp as soon as the last group has landed.
+              // sum_j w_j * ReLU(acc_j) with NCH independent FFMA2 chains per query.
+              const uint32_t taddr = tmem + lane_base + slot * pl.ncols + col0;
+  #pragma unroll
+              for (int gi = 0; gi < NGRP; ++gi) {
+                uint32_t cb[GRP / CK][CK];
+  #pragma unroll
+                for (int c = 0; c < GRP / CK; ++c) tmem_load_cols<CK>(taddr + gi * GRP + c * CK, cb[c]);
+  #pragma unroll
+                for (int c = 0; c < GRP / CK; ++c) tmem_wait_tied<CK>(cb[c]);
+                if (gi == NGRP - 1) {
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(bar_tempty(slot));   // slot free for the MMA warp
+                  PT_ADD(6);
+                  TRACE(6 + v, tcount, tid == 0);   // warpgroup v released the slot
+                }
+  #pragma unroll
+                for (int c = 0; c < GRP / CK; ++c) {
+  #pragma unroll
+                  for (int j4 = 0; j4 < CK / 4; ++j4) {
+                    const int col = gi * GRP + c * CK + 4 * j4;
+                    const int qi = col / H, hh = col % H;
+                    if (qi < qpw_eff) {
+                      const float4 wv = *reinterpret_cast<const float4*>(w_s + qi * H + hh);
+                      const uint32_t* x = cb[c] + 4 * j4;
+                      const float2 r0 = make_float2(fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
+                      const float2 r1 = make_float2(fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
+                      float2& pc = part[qi][(hh / 4) % NCH];
+                      pc = ffma2(make_float2(wv.x, wv.y), r0, pc);
+                      pc = ffma2(make_float2(wv.z, wv.w), r1, pc);
+                    }
                   }
                 }
               }
-            }
-#pragma unroll
-            for (int qi = 0; qi < QPW_MAX; ++qi) {
-              if (qi < qpw_eff) {
-                float sv = 0.f;
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) sv += part[qi][c].x + part[qi][c].y;
-                sv *= p.sm_scale;
-                const bool vis = s_idx <= vis_lim[qi];
-                bkey[b][qi] = orderable_key(sv);
-                bbal[b][qi] = __ballot_sync(0xffffffffu, vis && bkey[b][qi] > tau[qi]);
+  #pragma unroll
+              for (int qi = 0; qi < QPW_MAX; ++qi) {
+                if (qi < qpw_eff) {
+                  float sv = 0.f;
+  #pragma unroll
+                  for (int c = 0; c < NCH; ++c) sv += part[qi][c].x + part[qi][c].y;
+                  sv *= p.sm_scale;
+                  const bool vis = s_idx <= vis_lim[qi];
+                  bkey[b][qi] = orderable_key(sv);
+                  bbal[b][qi] = __ballot_sync(0xffffffffu, vis && bkey[b][qi] > tau[qi]);
+                }
               }
             }
             TRACE(10 + v, tcount, tid == 0);   // warpgroup v finished the tile's arithmetic
