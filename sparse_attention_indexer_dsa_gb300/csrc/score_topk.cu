@@ -932,20 +932,20 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               bbal[b][0] = __ballot_sync(0xffffffffu, vis && bkey[b][0] > tau[0]);
             } else {
               float2 part[QPW_MAX][NCH];
-  #pragma unroll
+#pragma unroll
               for (int qi = 0; qi < QPW_MAX; ++qi)
-  #pragma unroll
+#pragma unroll
                 for (int c = 0; c < NCH; ++c) part[qi][c] = make_float2(0.f, 0.f);
               // TMEM -> registers in groups of GRP columns (load, wait, reduce); the
               // slot goes back to the MMA warp as soon as the last group has landed.
               // sum_j w_j * ReLU(acc_j) with NCH independent FFMA2 chains per query.
               const uint32_t taddr = tmem + lane_base + slot * pl.ncols + col0;
-  #pragma unroll
+#pragma unroll
               for (int gi = 0; gi < NGRP; ++gi) {
                 uint32_t cb[GRP / CK][CK];
-  #pragma unroll
+#pragma unroll
                 for (int c = 0; c < GRP / CK; ++c) tmem_load_cols<CK>(taddr + gi * GRP + c * CK, cb[c]);
-  #pragma unroll
+#pragma unroll
                 for (int c = 0; c < GRP / CK; ++c) tmem_wait_tied<CK>(cb[c]);
                 if (gi == NGRP - 1) {
                   tc_fence_before();
@@ -954,9 +954,9 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
                   PT_ADD(6);
                   TRACE(6 + v, tcount, tid == 0);   // warpgroup v released the slot
                 }
-  #pragma unroll
+#pragma unroll
                 for (int c = 0; c < GRP / CK; ++c) {
-  #pragma unroll
+#pragma unroll
                   for (int j4 = 0; j4 < CK / 4; ++j4) {
                     const int col = gi * GRP + c * CK + 4 * j4;
                     const int qi = col / H, hh = col % H;
@@ -972,11 +972,11 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
                   }
                 }
               }
-  #pragma unroll
+#pragma unroll
               for (int qi = 0; qi < QPW_MAX; ++qi) {
                 if (qi < qpw_eff) {
                   float sv = 0.f;
-  #pragma unroll
+#pragma unroll
                   for (int c = 0; c < NCH; ++c) sv += part[qi][c].x + part[qi][c].y;
                   sv *= p.sm_scale;
                   const bool vis = s_idx <= vis_lim[qi];
@@ -1074,6 +1074,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
           count[qi] = kept;
         }
       }
+      PT_ADD(7);
 #pragma unroll
       for (int qi = 0; qi < QPW_MAX; ++qi) {
         const int tq = qbase + qi;

@@ -70,6 +70,49 @@ def test_integer_exact_mxfp8(H):
     np.testing.assert_array_equal(g_sc, ref["score"].astype(np.float32))
 
 
+@pytest.mark.parametrize("prec,k", [("bf16", 300), ("mxfp8", 300), ("mxfp8", 2048), ("bf16", 2048)])
+def test_integer_exact_long_documents(prec, k):
+    """Documents long enough that the candidate buffers hold thousands of
+    entries when a query's final selection runs (the sample-bracketed exact
+    select), with integer scores full of ties: still bit-exact, lowest index
+    first among equal scores.  The oracle checks a spread of rows."""
+    rng = np.random.default_rng(71 + k + (prec == "mxfp8"))
+    lens, H, D = [2600, 1500], 64, 128
+    T = sum(lens)
+    q = rng.integers(-3, 4, (T, H, D)).astype(np.float64)
+    kk = rng.integers(-3, 4, (T, D)).astype(np.float64)
+    w = rng.integers(-2, 3, (T, H)).astype(np.float32)
+    if prec == "mxfp8":
+        qc, qs, _ = O.quantize_mxfp8(q.reshape(T * H, D))
+        kc, ks, _ = O.quantize_mxfp8(kk)
+        args = (dev(qc), dev(qs), dev(kc), dev(ks))
+    else:
+        to_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # exact for small ints
+        args = (bf16_dev(to_bf16(q.reshape(T * H, D))), None, bf16_dev(to_bf16(kk)), None)
+    g_idx, g_sc, g_ln, cu = _run(*args, dev(w), lens, H, k, prec)
+    rows = np.concatenate([np.arange(0, 8), np.arange(1000, 1008), np.arange(2580, 2600), np.arange(2600, 2610),
+                           np.arange(T - 24, T)])
+    ref = O.indexer_topk(q, kk, w.astype(np.float64), cu, k, rows=rows)
+    np.testing.assert_array_equal(g_ln[rows], ref["len"])
+    np.testing.assert_array_equal(g_idx[rows], ref["idx"])
+    np.testing.assert_array_equal(g_sc[rows], ref["score"].astype(np.float32))
+
+
+def test_mxfp8_long_document_random():
+    """One 3000-token document at the target's shape (64 heads, top-2048):
+    every late query ends with a full candidate buffer."""
+    rng = np.random.default_rng(81)
+    lens, H, D, k = [3000], 64, 128, 2048
+    T = sum(lens)
+    qc, qs, qd = O.quantize_mxfp8(rng.standard_normal((T * H, D)))
+    kc, ks, kd = O.quantize_mxfp8(rng.standard_normal((T, D)))
+    w = (rng.standard_normal((T, H)) * 0.125).astype(np.float32)
+    g_idx, g_sc, g_ln, cu = _run(dev(qc), dev(qs), dev(kc), dev(ks), dev(w), lens, H, k, "mxfp8")
+    rows = np.concatenate([np.arange(2040, 2056), np.arange(T - 40, T)])
+    ref = O.indexer_topk(qd.reshape(T, H, D), kd, w.astype(np.float64), cu, k, rows=rows, with_scale=True)
+    compare_topk(g_idx, g_sc, g_ln, ref, REL_MXFP8, rows=rows)
+
+
 BF16_CASES = [
     # lens, H, D, k
     ([700], 64, 128, 64),
