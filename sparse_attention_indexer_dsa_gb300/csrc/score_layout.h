@@ -18,9 +18,9 @@ constexpr int kSfRawWords = 132;     // 128 scale words + up to 3 words of misal
 constexpr int kSfRawBytes = 640;     // kSfRawWords*4 = 528, padded to a 128-byte multiple
 constexpr int kSfTxBytes = 512;      // 32 rows x 16 bytes: the tcgen05.cp source layout
 constexpr int kMaxSmem = 232448;     // 227 KiB opt-in per block on sm_100/sm_103
-constexpr int kMiscInts = 320;       // per-warpgroup scratch ints
 constexpr int kBatch = 4;            // key tiles scored between two appends
 constexpr int kMaxQpw = 4;           // queries per epilogue warpgroup (at most)
+constexpr int kMiscInts = 192 + 2 * kBatch * kMaxQpw * 4;   // per-warpgroup scratch ints
 constexpr int kMaxStages = 6;
 constexpr int kMaxCand = 8192;      // candidate entries per query (at most)
 constexpr int kSfaCol = 384;         // MXFP8: key scales, 2 x 4 TMEM columns (alternating per tile)
@@ -32,6 +32,12 @@ constexpr int kSfbCol = 392;         // MXFP8: query scales, up to 2 atoms x 4 c
 __host__ __device__ constexpr int max_ncols(int prec) { return prec == PREC_BF16 ? 256 : 192; }
 __host__ __device__ constexpr int epi_wgs(int prec) { return prec == PREC_BF16 ? 4 : 3; }
 __host__ __device__ constexpr int score_threads(int prec) { return 64 + 128 * epi_wgs(prec); }
+// Batches between two abort / shrink votes.  Voting every other batch saves a
+// block-wide barrier per batch but needs room for two batches after a shrink:
+// only the MXFP8 64-head plan has candidate buffers large enough for that.
+__host__ __device__ constexpr int vote_every(int prec, int n_heads) {
+  return prec == PREC_MXFP8 && n_heads == 64 ? 2 : 1;
+}
 __host__ __device__ constexpr int qpw_max(int prec, int n_heads) {
   return max_ncols(prec) / (epi_wgs(prec) * n_heads) < kMaxQpw ? max_ncols(prec) / (epi_wgs(prec) * n_heads)
                                                                 : kMaxQpw;
@@ -135,7 +141,8 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
   const int elem = prec == PREC_BF16 ? 2 : 1;
   const bool sf = prec == PREC_MXFP8;
   s.chunks = head_dim * elem / kChunkBytes;
-  const int cand_min = round_up(keep + (kBatch + 2) * kTileKeys, 128);   // a full batch fits after a shrink
+  // every batch up to the next vote fits after a shrink
+  const int cand_min = round_up(keep + (kBatch * vote_every(prec, n_heads) + 2) * kTileKeys, 128);
   if (cand_min > kMaxCand) return false;
   const int cand_cap = 4 * keep > cand_min ? (4 * keep < kMaxCand ? round_up(4 * keep, 128) : kMaxCand) : cand_min;
   for (int qpw = qpw_max(prec, n_heads); qpw >= 1; qpw /= 2) {

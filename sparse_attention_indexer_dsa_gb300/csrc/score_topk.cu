@@ -281,10 +281,11 @@ enum {
   MS_MAX = 20,          // [4]
   MS_RCNT = 24,         // [2][8] per-warp counts of a compaction round
   MS_BCNT = 48,         // [2][kBatch][kMaxQpw][4] per-warp append counts of a batch
-  MS_CAND = 176,        // [2] the two sampled thresholds
-  MS_CNT4 = 180,        // [2][4] per-warp counts above the two sampled thresholds
-  MS_SORT = 192,        // [128] sample keys (sort exchange)
+  MS_CAND = MS_BCNT + 2 * kBatch * kMaxQpw * 4,   // [2] the two sampled thresholds
+  MS_CNT4 = MS_CAND + 4,                           // [2][4] per-warp counts above them
+  MS_SORT = MS_CNT4 + 12,                          // [128] sample keys (sort exchange)
 };
+static_assert(MS_SORT + 128 <= kMiscInts, "per-warpgroup scratch ints");
 
 // Shrink the n candidates of one query (n > keep).  The buffer holds
 // orderable score keys in index order.  Radix select on key - kmin, 8-bit
@@ -563,6 +564,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
   constexpr int NGRP = NCOLW / GRP;
   constexpr int NCH = (H / 4) < 4 ? (H / 4) : 4;     // independent FFMA2 chains per query
   constexpr bool FRAG = QPW_MAX == 1 && H == 64;      // one query of 64 heads per warpgroup
+  constexpr int VOTE = vote_every(PREC, H);            // batches between two votes
   static_assert(QPW_MAX >= 1 && QPW_MAX <= kMaxQpw, "queries per warpgroup");
   const ScorePlan& pl = p.plan;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1023,16 +1025,21 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         PT_ADD(2);
         TRACE(9, nbatch, tid == 0 && v == 0 && EW < 4);   // batch appended
         // ---- room for the next batch, or shrink: all warpgroups together ----
-        // One vote over every epilogue thread decides, uniformly, whether to
-        // abort and whether to shrink; shrinking in lockstep lets the queries'
-        // compactions overlap instead of stalling the shared TMEM ring one
-        // after another.  One barrier carries both votes: lane 0 of each warp
-        // reports an abort, lanes 1..31 a shrink, so the count it returns is
-        // (warps aborting) + 31 * (warps needing room), with at most 16 warps.
+        // Every VOTE-th batch of the item, one vote over every epilogue
+        // thread decides, uniformly, whether to abort and whether to shrink
+        // (room for the batches up to the next vote); shrinking in lockstep
+        // lets the queries' compactions overlap instead of stalling the shared
+        // TMEM ring one after another.  One barrier carries both votes: lane 0
+        // of each warp reports an abort, lanes 1..31 a shrink, so the count it
+        // returns is (warps aborting) + 31 * (warps needing room), with at most
+        // 16 warps.  The item's last batch needs no vote: the final selection
+        // follows, and an abort is caught at the next item's first vote.
+        PT_ADD(3);
+        if ((tb / kBatch) % VOTE != VOTE - 1 || tb + kBatch >= m.ntiles) continue;
         bool need = false;
 #pragma unroll
         for (int qi = 0; qi < QPW_MAX; ++qi)
-          need |= qi < qpw_eff && count[qi] + kBatch * kTileKeys > C;
+          need |= qi < qpw_eff && count[qi] + VOTE * kBatch * kTileKeys > C;
         need = __any_sync(0xffffffffu, need);
         const bool warp_abort = __any_sync(0xffffffffu, !ok_all || *abort_flag);
         const int votes = named_bar_popc(bar_all, EW * 128, lane == 0 ? warp_abort : need);
@@ -1046,7 +1053,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
           for (int qi = 0; qi < QPW_MAX; ++qi) {
             if (qi < qpw_eff && count[qi] > keep + kTileKeys) {
               named_bar_sync(bar_id, 128);   // appends visible to the whole warpgroup
-              const int cap = C - (kBatch + 2) * kTileKeys;
+              const int cap = C - (VOTE * kBatch + 2) * kTileKeys;
               int kept;
               uint32_t th;
               if (wg_shrink_sampled(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, cap, wq,
