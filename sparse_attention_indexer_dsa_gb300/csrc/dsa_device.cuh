@@ -341,6 +341,16 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Predicated shared-memory stores (no branch around them).
+__device__ __forceinline__ void st_shared_u32_if(bool p, uint32_t addr, uint32_t v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.u32 [%0], %1;\n\t}"
+               ::"r"(addr), "r"(v), "r"((uint32_t)p) : "memory");
+}
+__device__ __forceinline__ void st_shared_u16_if(bool p, uint32_t addr, uint16_t v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.u16 [%0], %1;\n\t}"
+               ::"r"(addr), "h"(v), "r"((uint32_t)p) : "memory");
+}
+
 // Barrier over `nthreads` threads that also counts the threads whose
 // predicate is true.
 __device__ __forceinline__ int named_bar_popc(int id, int nthreads, bool pred) {

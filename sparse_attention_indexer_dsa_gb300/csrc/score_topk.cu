@@ -809,6 +809,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
     const int col0 = lq0 * H;                     // their first accumulator column
     uint32_t* ckey_base = reinterpret_cast<uint32_t*>(smem + pl.cand_key_off) + lq0 * C;
     uint16_t* cidx_base = reinterpret_cast<uint16_t*>(smem + pl.cand_idx_off) + lq0 * C;
+    const uint32_t ckey_s = smem_u32(ckey_base), cidx_s = smem_u32(cidx_base);   // shared-window addresses
     float* w_s = reinterpret_cast<float*>(smem + pl.w_off) + lq0 * H;
     int* hist = reinterpret_cast<int*>(smem + pl.hist_off) + v * 256;
     int* ms = reinterpret_cast<int*>(smem + pl.misc_off) + v * kMiscInts;
@@ -1013,11 +1014,10 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
               const int before = (wq > 0 ? cc[b].x : 0) + (wq > 1 ? cc[b].y : 0) + (wq > 2 ? cc[b].z : 0);
-              if ((bbal[b][qi] >> lane) & 1u) {
-                const int pos = count[qi] + before + __popc(bbal[b][qi] & lt);
-                ckey_base[qi * C + pos] = bkey[b][qi];
-                cidx_base[qi * C + pos] = (uint16_t)((tb + b) * kTileKeys + row);
-              }
+              const bool mine = (bbal[b][qi] >> lane) & 1u;
+              const int pos = qi * C + count[qi] + before + __popc(bbal[b][qi] & lt);
+              st_shared_u32_if(mine, ckey_s + 4u * (uint32_t)pos, bkey[b][qi]);
+              st_shared_u16_if(mine, cidx_s + 2u * (uint32_t)pos, (uint16_t)((tb + b) * kTileKeys + row));
               count[qi] += cc[b].x + cc[b].y + cc[b].z + cc[b].w;
             }
           }
