@@ -420,11 +420,10 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
       const bool e1 = (be[m] >> lane) & 1u;
       const int my_g = gb + __popc(bg[m] & lt);
       const int my_e = eb + __popc(be[m] & lt);
-      if (g1 || (e1 && my_e < keep_eq)) {
-        const int pos = my_g + (my_e < keep_eq ? my_e : keep_eq);   // kept entries before it
-        keys[pos] = rk[m];
-        idx[pos] = ri[m];
-      }
+      const bool kp = g1 || (e1 && my_e < keep_eq);
+      const int pos = my_g + (my_e < keep_eq ? my_e : keep_eq);   // kept entries before it
+      st_shared_u32_if(kp, smem_u32(keys) + 4u * (uint32_t)pos, rk[m]);
+      st_shared_u16_if(kp, smem_u32(idx) + 2u * (uint32_t)pos, ri[m]);
       gb += __popc(bg[m]);
       eb += __popc(be[m]);
     }
@@ -534,11 +533,10 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      if ((bk[m] >> lane) & 1u) {
-        const int pos = base + __popc(bk[m] & lt);
-        keys[pos] = rk[m];
-        idx[pos] = ri[m];
-      }
+      const bool kp = (bk[m] >> lane) & 1u;
+      const int pos = base + __popc(bk[m] & lt);
+      st_shared_u32_if(kp, smem_u32(keys) + 4u * (uint32_t)pos, rk[m]);
+      st_shared_u16_if(kp, smem_u32(idx) + 2u * (uint32_t)pos, ri[m]);
       base += __popc(bk[m]);
     }
     out += tot;
