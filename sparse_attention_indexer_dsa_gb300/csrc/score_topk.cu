@@ -287,6 +287,12 @@ enum {
 };
 static_assert(MS_SORT + 128 <= kMiscInts, "per-warpgroup scratch ints");
 
+// Compactions move PER entries per thread per round (one warpgroup barrier
+// per 128 * PER entries): 8 where the block has 128 registers a thread, 4
+// where it has 96.
+template <int PREC>
+__host__ __device__ constexpr int compact_per() { return score_threads(PREC) <= 448 ? 8 : 4; }
+
 // Shrink the n candidates of one query (n > keep).  The buffer holds
 // orderable score keys in index order.  Radix select on key - kmin, 8-bit
 // digits from the highest bit in which the buffer's keys differ:
@@ -299,16 +305,23 @@ static_assert(MS_SORT + 128 <= kMiscInts, "per-warpgroup scratch ints");
 //    the bin's lower edge minus one, a threshold no larger than the true
 //    keep-th key, so no member of the final top-k is ever rejected.
 // Histogram passes re-read the keys from shared memory; the stable in-place
-// compaction runs in rounds of 512 entries (writes of a round land below the
+// compaction runs in rounds of 128 * PER entries (writes of a round land below the
 // next round's inputs).  *count_out receives the number kept.  All 128
 // threads of the warpgroup.
+template <int PER>
 __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n, int keep,
                                            bool exact, int cap_after, int wq, uint32_t lane,
                                            int* hist, int* ms, int bar_id, int* count_out) {
   const int tid = wq * 32 + (int)lane;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int e = tid; e < n; e += 128) {
-    const uint32_t k = keys[e];
+  int e0 = tid;
+  for (; e0 + 384 < n; e0 += 512) {
+    const uint32_t k0 = keys[e0], k1 = keys[e0 + 128], k2 = keys[e0 + 256], k3 = keys[e0 + 384];
+    kmin = min(kmin, min(min(k0, k1), min(k2, k3)));
+    kmax = max(kmax, max(max(k0, k1), max(k2, k3)));
+  }
+  for (; e0 < n; e0 += 128) {
+    const uint32_t k = keys[e0];
     kmin = min(kmin, k);
     kmax = max(kmax, k);
   }
@@ -378,21 +391,27 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
     }
     shift = shift > 8 ? shift - 8 : 0;
   }
-  // stable compaction in rounds of 512: keep (rel & pmask) > prefix, and the
-  // first keep_eq (in buffer order) with == prefix
+  // stable compaction in rounds of 128 * PER: keep (rel & pmask) > prefix,
+  // and the first keep_eq (in buffer order) with == prefix
   const uint32_t lt = (1u << lane) - 1u;
+  const uint32_t keys_s = smem_u32(keys), idx_s = smem_u32(idx);
   int out = 0, eq_seen = 0;
-  for (int r0 = 0, rnd = 0; r0 < n; r0 += 512, ++rnd) {
-    uint32_t rk[4];
-    uint16_t ri[4];
-    uint32_t bg[4], be[4];
+  for (int r0 = 0, rnd = 0; r0 < n; r0 += (128 * PER), ++rnd) {
+    uint32_t rk[PER];
+    uint16_t ri[PER];
+    uint32_t bg[PER], be[PER];
     int gt = 0, eq = 0;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int e = r0 + wq * 128 + m * 32 + (int)lane;
+    for (int m = 0; m < PER; ++m) {
+      const int e = r0 + wq * (32 * PER) + m * 32 + (int)lane;
       const bool v = e < n;
       rk[m] = v ? keys[e] : 0u;
       ri[m] = v ? idx[e] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int e = r0 + wq * (32 * PER) + m * 32 + (int)lane;
+      const bool v = e < n;
       const uint32_t mk = (rk[m] - kmin) & pmask;
       bg[m] = __ballot_sync(0xffffffffu, v && mk > prefix);
       be[m] = __ballot_sync(0xffffffffu, v && mk == prefix);
@@ -415,15 +434,15 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
       etot += rc[4 + w];
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < PER; ++m) {
       const bool g1 = (bg[m] >> lane) & 1u;
       const bool e1 = (be[m] >> lane) & 1u;
       const int my_g = gb + __popc(bg[m] & lt);
       const int my_e = eb + __popc(be[m] & lt);
       const bool kp = g1 || (e1 && my_e < keep_eq);
       const int pos = my_g + (my_e < keep_eq ? my_e : keep_eq);   // kept entries before it
-      st_shared_u32_if(kp, smem_u32(keys) + 4u * (uint32_t)pos, rk[m]);
-      st_shared_u16_if(kp, smem_u32(idx) + 2u * (uint32_t)pos, ri[m]);
+      st_shared_u32_if(kp, keys_s + 4u * (uint32_t)pos, rk[m]);
+      st_shared_u16_if(kp, idx_s + 2u * (uint32_t)pos, ri[m]);
       gb += __popc(bg[m]);
       eb += __popc(be[m]);
     }
@@ -445,6 +464,7 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
 // radix select.  On success
 // *tau_out is the new acceptance threshold (candidate - 1: later keys equal to
 // it are still accepted, so nothing that may belong to the top-k is lost).
+template <int PER>
 __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, int n, int keep,
                                                int cap_after, int wq, uint32_t lane, int* ms,
                                                int bar_id, uint32_t* tau_out, int* count_out) {
@@ -485,7 +505,13 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
   named_bar_sync(bar_id, 128);
   const uint32_t cand_a = (uint32_t)ms[MS_CAND], cand_s = (uint32_t)ms[MS_CAND + 1];
   int ca = 0, cs = 0;
-  for (int e = tid; e < n; e += 128) {
+  int e = tid;
+  for (; e + 384 < n; e += 512) {
+    const uint32_t k0 = keys[e], k1 = keys[e + 128], k2 = keys[e + 256], k3 = keys[e + 384];
+    ca += (k0 >= cand_a) + (k1 >= cand_a) + (k2 >= cand_a) + (k3 >= cand_a);
+    cs += (k0 >= cand_s) + (k1 >= cand_s) + (k2 >= cand_s) + (k3 >= cand_s);
+  }
+  for (; e < n; e += 128) {
     const uint32_t kv = keys[e];
     ca += kv >= cand_a ? 1 : 0;
     cs += kv >= cand_s ? 1 : 0;
@@ -507,20 +533,25 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
     cand = cand_s;
   else
     return false;
-  // stable compaction in rounds of 512 entries
+  // stable compaction in rounds of 128 * PER entries
   const uint32_t lt = (1u << lane) - 1u;
+  const uint32_t keys_s = smem_u32(keys), idx_s = smem_u32(idx);
   int out = 0;
-  for (int r0 = 0, rnd = 0; r0 < n; r0 += 512, ++rnd) {
-    uint32_t rk[4], bk[4];
-    uint16_t ri[4];
+  for (int r0 = 0, rnd = 0; r0 < n; r0 += (128 * PER), ++rnd) {
+    uint32_t rk[PER], bk[PER];
+    uint16_t ri[PER];
     int cnt = 0;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int e = r0 + wq * 128 + m * 32 + (int)lane;
+    for (int m = 0; m < PER; ++m) {
+      const int e = r0 + wq * (32 * PER) + m * 32 + (int)lane;
       const bool v = e < n;
       rk[m] = v ? keys[e] : 0u;
       ri[m] = v ? idx[e] : (uint16_t)0;
-      bk[m] = __ballot_sync(0xffffffffu, v && rk[m] >= cand);
+    }
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int e = r0 + wq * (32 * PER) + m * 32 + (int)lane;
+      bk[m] = __ballot_sync(0xffffffffu, e < n && rk[m] >= cand);
       cnt += __popc(bk[m]);
     }
     int* rc = ms + MS_RCNT + (rnd & 1) * 8;
@@ -532,11 +563,11 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
       tot += rc[w];
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < PER; ++m) {
       const bool kp = (bk[m] >> lane) & 1u;
       const int pos = base + __popc(bk[m] & lt);
-      st_shared_u32_if(kp, smem_u32(keys) + 4u * (uint32_t)pos, rk[m]);
-      st_shared_u16_if(kp, smem_u32(idx) + 2u * (uint32_t)pos, ri[m]);
+      st_shared_u32_if(kp, keys_s + 4u * (uint32_t)pos, rk[m]);
+      st_shared_u16_if(kp, idx_s + 2u * (uint32_t)pos, ri[m]);
       base += __popc(bk[m]);
     }
     out += tot;
@@ -1054,11 +1085,11 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               const int cap = C - (VOTE * kBatch + 2) * kTileKeys;
               int kept;
               uint32_t th;
-              if (wg_shrink_sampled(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, cap, wq,
+              if (wg_shrink_sampled<compact_per<PREC>()>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, cap, wq,
                                     lane, ms, bar_id, &th, &kept)) {
                 tau[qi] = th;
               } else {
-                tau[qi] = wg_select(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, false,
+                tau[qi] = wg_select<compact_per<PREC>()>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, false,
                                     cap, wq, lane, hist, ms, bar_id, &kept);
               }
               count[qi] = kept;
@@ -1074,7 +1105,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
       for (int qi = 0; qi < QPW_MAX; ++qi) {
         if (qi < qpw_eff && count[qi] > keep) {
           int kept;
-          wg_select(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, true, keep, wq, lane, hist,
+          wg_select<compact_per<PREC>()>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, true, keep, wq, lane, hist,
                     ms, bar_id, &kept);
           count[qi] = kept;
         }
