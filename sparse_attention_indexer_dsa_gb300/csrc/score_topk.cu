@@ -346,7 +346,16 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
   for (;;) {
     for (int b = tid; b < 256; b += 128) hist[b] = 0;
     named_bar_sync(bar_id, 128);
-    for (int e = tid; e < n; e += 128) {
+    int e = tid;
+    for (; e + 384 < n; e += 512) {
+      uint32_t rel[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) rel[u] = keys[e + 128 * u] - kmin;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if ((rel[u] & pmask) == prefix) atomicAdd(&hist[(rel[u] >> shift) & 0xFFu], 1);
+    }
+    for (; e < n; e += 128) {
       const uint32_t rel = keys[e] - kmin;
       if ((rel & pmask) == prefix) atomicAdd(&hist[(rel >> shift) & 0xFFu], 1);
     }
