@@ -341,19 +341,24 @@ def _finish_row(chosen, scores, width: int, order: str):
 
 def indexer_topk(q_op, k_op, w, cu_seqlens, index_topk: int, sm_scale: float = 1.0,
                  rows: Optional[Sequence[int]] = None, order: str = "index",
-                 with_scale: bool = False):
+                 with_scale: bool = False, cu_seqlens_k=None):
     """Top-k per query over its causally visible keys.
 
-    q_op [T, H, D], k_op [T, D]: scoring operands (already rounded /
-    dequantised); w [T, H]; cu_seqlens [B+1].  Query t (local position p in
-    its document starting at token a) sees keys a .. a+p (diagonal included).
-    Selected indices are local to the document; fewer than k visible keys ->
-    -1 / -inf padding and len = p + 1.  order "index": ascending index (the
-    library's default row order); "score": (score desc, index asc).
-    Returns dict(rows, idx [R, k], score [R, k], len [R], and when with_scale
-    all_scores / all_scales: lists of the full score and error-scale rows).
+    q_op [T, H, D], k_op [S, D]: scoring operands (already rounded /
+    dequantised); w [T, H]; cu_seqlens [B+1] for the queries and, when
+    given, cu_seqlens_k [B+1] for the keys (default: the same).  Document d
+    has T_d queries and S_d >= T_d keys; its queries are its last T_d tokens,
+    so query i of it sits at position p = S_d - T_d + i (the global causal
+    offset of [P1] review finding 2) and sees local keys 0 .. p (diagonal
+    included).  Selected indices are local to the document's keys; fewer than
+    k visible keys -> -1 / -inf padding and len = p + 1.  order "index":
+    ascending index (the library's default row order); "score": (score desc,
+    index asc).  Returns dict(rows, idx [R, k], score [R, k], len [R], and
+    when with_scale all_scores / all_scales: lists of the full score and
+    error-scale rows).
     """
     cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cuk = cu if cu_seqlens_k is None else np.asarray(cu_seqlens_k, dtype=np.int64)
     T = int(cu[-1])
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     doc_of = np.searchsorted(cu, rows, side="right") - 1
@@ -364,8 +369,10 @@ def indexer_topk(q_op, k_op, w, cu_seqlens, index_topk: int, sm_scale: float = 1
     all_scores, all_scales = [], []
     for r, (t, d) in enumerate(zip(rows, doc_of)):
         a = cu[d]
-        p = t - a
-        kv = k_op[a:t + 1]
+        off = (cuk[d + 1] - cuk[d]) - (cu[d + 1] - cu[d])
+        assert off >= 0, "a document has more queries than keys"
+        p = off + t - a
+        kv = k_op[cuk[d]:cuk[d] + p + 1]
         s = indexer_scores(q_op[t], kv, w[t], sm_scale)
         chosen = select_topk(s, index_topk)
         out_idx[r], out_sc[r], out_len[r] = _finish_row(chosen, s, index_topk, order)

@@ -8,7 +8,7 @@ import oracle.dsa_oracle as O
 import sparse_attention_indexer_dsa_gb300 as dsa
 from sparse_attention_indexer_dsa_gb300 import workloads as W
 from tests.gpu_util import bf16_dev, dev, host
-from tests.parity import REL_BF16, compare_topk
+from tests.parity import REL_BF16, REL_MXFP8, compare_topk
 
 pytestmark = pytest.mark.gpu
 
@@ -56,3 +56,27 @@ def test_kpool_workload_end_to_end():
                        wl.cu_seqlens, rcp, wl.index_topk, P, True, rows=rows, with_scale=True)
     # pooled keys differ by at most one BF16 ulp between the two sides
     compare_topk(host(idx), host(sc), host(ln), ref, REL_BF16 + 2.0 ** -8, pool=P, tail=True, rows=rows)
+
+
+def test_kpool_mxfp8_scoring():
+    """KPool with MXFP8 scoring: the pooled BF16 keys are quantised to MXFP8
+    (dsa_idx_quantize_mxfp8) and scored against MXFP8 queries in pool mode.
+    The oracle quantises its own pooled keys the same way; the two sides'
+    pooled keys may differ by one BF16 ulp, which can move a key element by
+    one E4M3 step, hence the slack on top of the MXFP8 tolerance."""
+    wl = W.Workload("kpool-mx", [2600, 700], 64, 128, 2048, "mxfp8", "normal", w_std=0.125, kpool=4, seed=1007)
+    x = W.make_inputs(wl)
+    T, H, D, P = wl.total_tokens, wl.n_heads, wl.head_dim, wl.kpool
+    cu = dev(wl.cu_seqlens)
+    kp, cp = dsa.kpool_compress(dev(x["k"]), dev(x["gate_bits"].view(np.int16)), dev(x["slot_bias"]), cu, P)
+    kc, ks = dsa.quantize_mxfp8(kp)
+    qc, qs = dsa.quantize_mxfp8(dev(x["q"].reshape(T * H, D)))
+    idx, sc, ln = dsa.score_topk(qc, qs, kc, ks, dev(x["w"]), cu, wl.max_seqlen, H, wl.index_topk, "mxfp8",
+                                 kpool_size=P, cu_pools=cp, tail=True)
+    kbar, rcp = O.kpool_compress(x["k"], O.bf16_bits_to_float(x["gate_bits"]), x["slot_bias"], wl.cu_seqlens, P)
+    _, _, kq = O.quantize_mxfp8(O.round_bf16(kbar))
+    _, _, qq = O.quantize_mxfp8(x["q"].reshape(T * H, D).astype(np.float64))
+    rows = np.concatenate([np.arange(0, 40), np.arange(2560, 2620), np.arange(T - 40, T)])
+    ref = O.kpool_topk(qq.reshape(T, H, D), kq, x["w"].astype(np.float64), wl.cu_seqlens, rcp, wl.index_topk, P,
+                       True, rows=rows, with_scale=True)
+    compare_topk(host(idx), host(sc), host(ln), ref, REL_MXFP8 + 2.0 ** -6, pool=P, tail=True, rows=rows)

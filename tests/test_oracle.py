@@ -367,6 +367,50 @@ def test_thd_documents_equal_separate_runs():
         np.testing.assert_array_equal(r["score"][a:a + L], rd["score"])
 
 
+def test_global_offsets_equal_last_rows_of_full_run():
+    """Queries that are the last T_d of S_d tokens ([P1] review finding 2,
+    global causal offsets) score exactly like those rows of the full
+    self-attention run over all S_d tokens."""
+    rng = np.random.default_rng(19)
+    lens_k, lens_q = [12, 7, 4, 9], [5, 7, 0, 1]
+    S = sum(lens_k)
+    q_full = rng.integers(-2, 3, (S, 3, 8)).astype(np.float64)   # integers: ties exercise the rule
+    k = rng.integers(-2, 3, (S, 8)).astype(np.float64)
+    w_full = rng.integers(-2, 3, (S, 3)).astype(np.float64)
+    cuk = np.concatenate([[0], np.cumsum(lens_k)])
+    cuq = np.concatenate([[0], np.cumsum(lens_q)])
+    rows_full = np.concatenate([np.arange(cuk[d + 1] - lens_q[d], cuk[d + 1]) for d in range(4)]).astype(np.int64)
+    full = O.indexer_topk(q_full, k, w_full, cuk, 6, rows=rows_full)
+    off = O.indexer_topk(q_full[rows_full], k, w_full[rows_full], cuq, 6, cu_seqlens_k=cuk)
+    np.testing.assert_array_equal(off["idx"], full["idx"])
+    np.testing.assert_array_equal(off["score"], full["score"])
+    np.testing.assert_array_equal(off["len"], full["len"])
+
+
+def test_global_offsets_brute_force():
+    """Explicit loops: query i of document d sees keys 0 .. S_d - T_d + i of
+    that document; the best min(k, visible) by (score desc, index asc),
+    listed in ascending index."""
+    rng = np.random.default_rng(20)
+    lens_k, lens_q = [6, 3], [2, 3]
+    q = rng.standard_normal((5, 2, 4))
+    k = rng.standard_normal((9, 4))
+    w = rng.standard_normal((5, 2))
+    cuk, cuq = [0, 6, 9], [0, 2, 5]
+    r = O.indexer_topk(q, k, w, cuq, 3, cu_seqlens_k=cuk)
+    row = 0
+    for d in range(2):
+        for i in range(lens_q[d]):
+            p = lens_k[d] - lens_q[d] + i
+            sc = _brute_scores(q[row], k[cuk[d]:cuk[d] + p + 1], w[row], 1.0)
+            best = sorted(range(p + 1), key=lambda s_: (-sc[s_], s_))[:3]
+            n = len(best)
+            assert r["len"][row] == n
+            np.testing.assert_array_equal(r["idx"][row][:n], sorted(best))
+            np.testing.assert_allclose(r["score"][row][:n], sc[sorted(best)], rtol=1e-12)
+            row += 1
+
+
 # ----------------------------------------------------------------- KPool
 
 def test_kpool_single_slot_reduces_to_plain_indexer():
