@@ -204,6 +204,32 @@ dsa_status_t dsa_idx_score_topk(
     int32_t* topk_idx, float* topk_score, int32_t* topk_len,
     void* ws, size_t ws_bytes, dsa_stream_t stream);
 
+/* Fused score + top-k for documents whose queries are the last tokens of a
+ * longer key sequence ([P1] review finding 2: "global causal offsets", e.g.
+ * a query chunk scored against its document's keys so far).  Document d has
+ * T_d = cu_seqlens_q[d+1]-cu_seqlens_q[d] queries and S_d =
+ * cu_seqlens_k[d+1]-cu_seqlens_k[d] >= T_d keys; its query i sits at position
+ * S_d - T_d + i and sees keys 0 .. S_d - T_d + i of the document.
+ *   q, q_scale, w, topk_idx, topk_score, topk_len  as in dsa_idx_score_topk,
+ *               with total_q rows (tokens)
+ *   k, k_scale  [total_k, head_dim] (and [total_k, head_dim/32])
+ *   cu_seqlens_q, cu_seqlens_k  device int32 [num_seqs+1] each
+ *   max_seqlen_q, max_seqlen_k  upper bounds of T_d and S_d (S_d <= 65536)
+ *   ws, ws_bytes  dsa_idx_workspace_size() with total_tokens =
+ *               max(total_q, total_k)
+ * Indices are local to the document's keys.  Pool mode is not available
+ * here.  T_d > S_d (or inconsistent prefixes) is caught on the device:
+ * DSA_ERR_INVALID_ARG in the status word, no output written.  Equal key and
+ * query lengths give exactly dsa_idx_score_topk's result. */
+dsa_status_t dsa_idx_score_topk_kv(
+    const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
+    const void* w, dsa_dtype_t w_dtype, float sm_scale,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+    int n_heads, int head_dim, int index_topk, dsa_precision_t prec, int flags,
+    int32_t* topk_idx, float* topk_score, int32_t* topk_len,
+    void* ws, size_t ws_bytes, dsa_stream_t stream);
+
 /* Allocation-free dsa_idx_score_topk, for callers that cannot provide device
  * scratch memory: code that runs after a no-allocation-past-start-up point
  * (latency-critical serving loops, real-time pipelines), hosts whose device

@@ -18,7 +18,7 @@ from ._abi import (DSA_FLAG_DETERMINISTIC, DSA_FLAG_KPOOL_TAIL, DSA_FLAG_SORT_BY
                    DSA_PREC_BF16, DSA_PREC_MXFP8)
 
 __all__ = [
-    "DsaError", "preprocess", "quantize_mxfp8", "kpool_compress", "score_topk", "workspace",
+    "DsaError", "preprocess", "quantize_mxfp8", "kpool_compress", "score_topk", "score_topk_kv", "workspace",
     "read_status", "debug_mma_tile", "output_width",
 ]
 
@@ -169,6 +169,38 @@ def score_topk(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: torch.
         _ptr(cu_seqlens), B, T, max_seqlen, n_heads, D, index_topk, _prec(prec), flags, kpool_size,
         _ptr(cu_pools), _ptr(idx), _ptr(sc), _ptr(lens), _ptr(ws), ws.numel(), _stream())
     _check(code, "dsa_idx_score_topk")
+    return idx, sc, lens
+
+
+def score_topk_kv(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: torch.Tensor,
+                  k_scale: Optional[torch.Tensor], w: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                  cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, n_heads: int,
+                  index_topk: int, prec="bf16", sm_scale: float = 1.0, return_scores: bool = True,
+                  ws: Optional[torch.Tensor] = None, out=None):
+    """Fused score + top-k with more keys than queries per document
+    (dsa_idx_score_topk_kv): document d's queries are its last T_d tokens.
+
+    q_op [Tq*H, D], k_op [Tk, D], w [Tq, H].  Returns (idx int32 [Tq, k],
+    scores fp32 [Tq, k] or None, lens int32 [Tq]); indices are local to the
+    document's keys."""
+    Tq, Tk = w.shape[0], k_op.shape[0]
+    D = q_op.shape[-1]
+    B = cu_seqlens_q.numel() - 1
+    if out is None:
+        idx = torch.empty((Tq, index_topk), dtype=torch.int32, device=q_op.device)
+        sc = torch.empty((Tq, index_topk), dtype=torch.float32, device=q_op.device) if return_scores else None
+        lens = torch.empty((Tq,), dtype=torch.int32, device=q_op.device)
+    else:
+        idx, sc, lens = out
+    if ws is None:
+        ws = workspace(max(Tq, Tk), B, max(max_seqlen_q, max_seqlen_k), n_heads, D, index_topk, 1, prec,
+                       q_op.device)
+    code = _abi.load().dsa_idx_score_topk_kv(
+        _ptr(q_op), _ptr(q_scale), _ptr(k_op), _ptr(k_scale), _ptr(w), _dtype(w), sm_scale,
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Tq, Tk, max_seqlen_q, max_seqlen_k, n_heads, D,
+        index_topk, _prec(prec), DSA_FLAG_DETERMINISTIC, _ptr(idx), _ptr(sc), _ptr(lens), _ptr(ws),
+        ws.numel(), _stream())
+    _check(code, "dsa_idx_score_topk_kv")
     return idx, sc, lens
 
 

@@ -49,6 +49,9 @@ SIGNATURES = {
     "dsa_idx_score_topk": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                     _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "dsa_idx_score_topk_kv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_f, _vp, _vp, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _vp, _vp, _vp, _vp, _c_size, _vp]),
     "dsa_idx_score_topk_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                             _vp, _vp, _vp, _vp]),

@@ -269,17 +269,24 @@ dsa_status_t dsa_idx_kpool_compress(const void* k, dsa_dtype_t k_dtype, const ui
   return DSA_OK;
 }
 
-dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const void* k,
-                                const uint8_t* k_scale, const void* w, dsa_dtype_t w_dtype,
-                                float sm_scale, const int32_t* cu_seqlens, int num_seqs,
-                                int total_tokens, int max_seqlen, int n_heads, int head_dim,
-                                int index_topk, dsa_precision_t prec, int flags, int kpool_size,
-                                const int32_t* cu_pools, int32_t* topk_idx, float* topk_score,
-                                int32_t* topk_len, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+namespace {
+
+// The fused call for self-attention documents (cu_k == nullptr: every
+// document has as many keys as queries) or for documents whose queries are
+// the last tokens of a longer key sequence (cu_k, total_k, max_seqlen_k).
+dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
+                             const void* w, dsa_dtype_t w_dtype, float sm_scale, const int32_t* cu_seqlens,
+                             const int32_t* cu_k, int num_seqs, int total_tokens, int total_k,
+                             int max_seqlen, int max_seqlen_k, int n_heads, int head_dim, int index_topk,
+                             dsa_precision_t prec, int flags, int kpool_size, const int32_t* cu_pools,
+                             int32_t* topk_idx, float* topk_score, int32_t* topk_len, void* ws,
+                             size_t ws_bytes, dsa_stream_t stream) {
   if (!q || !k || !w || !cu_seqlens || !topk_idx) return fail(DSA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(k)) return fail(DSA_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
-  if (num_seqs < 1 || total_tokens < 0 || max_seqlen < 0) return fail(DSA_ERR_INVALID_ARG, "sizes");
-  if (max_seqlen > 65536) return fail(DSA_ERR_UNSUPPORTED, "max_seqlen above 65536");
+  if (num_seqs < 1 || total_tokens < 0 || max_seqlen < 0 || total_k < 0 || max_seqlen_k < 0)
+    return fail(DSA_ERR_INVALID_ARG, "sizes");
+  if (max_seqlen > 65536 || max_seqlen_k > 65536) return fail(DSA_ERR_UNSUPPORTED, "max_seqlen above 65536");
+  if (cu_k && kpool_size > 1) return fail(DSA_ERR_UNSUPPORTED, "pool mode with separate key lengths");
   if (!heads_ok(n_heads)) return fail(DSA_ERR_UNSUPPORTED, "n_heads must be 4, 8, 16, 32 or 64");
   if (prec != DSA_PREC_BF16 && prec != DSA_PREC_MXFP8) return fail(DSA_ERR_INVALID_ARG, "prec");
   if (prec == DSA_PREC_MXFP8) {
@@ -305,8 +312,9 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   if (keep < 1) return fail(DSA_ERR_INVALID_ARG, "index_topk / kpool_size must be >= 1");
   if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
   const bool mxw = prec == DSA_PREC_MXFP8;
-  if (ws_bytes < ws_total(total_tokens, num_seqs, mxw))
-    return fail(DSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, ws_total(total_tokens, num_seqs, mxw));
+  const int ws_tokens = total_k > total_tokens ? total_k : total_tokens;   // workspace sizing unit
+  if (ws_bytes < ws_total(ws_tokens, num_seqs, mxw))
+    return fail(DSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, ws_total(ws_tokens, num_seqs, mxw));
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(DSA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   ScoreParams p{};
   const int pl_prec = prec == DSA_PREC_MXFP8 ? PREC_MXFP8 : PREC_BF16;
@@ -316,7 +324,7 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   dsa_status_t s = device_info(&di);
   if (s != DSA_OK) return s;
   const bool fp8 = pl_prec == PREC_MXFP8;
-  const int64_t krows = kpool_size > 1 ? total_tokens / kpool_size : total_tokens;
+  const int64_t krows = kpool_size > 1 ? total_tokens / kpool_size : total_k;
   if ((s = make_operand_map(&p.tm_q, q, (int64_t)total_tokens * n_heads, head_dim, fp8, p.plan.ncols)) != DSA_OK)
     return s;
   if ((s = make_operand_map(&p.tm_k, k, krows, head_dim, fp8)) != DSA_OK) return s;
@@ -329,12 +337,13 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   int* doc_prefix = reinterpret_cast<int*>(wsb + ws_prefix_off());
   int* tile_base = reinterpret_cast<int*>(wsb + ws_tiles_off(num_seqs));
   int2* items = reinterpret_cast<int2*>(wsb + ws_items_off(num_seqs));
-  uint32_t* ksf_tiles = reinterpret_cast<uint32_t*>(wsb + ws_ksf_off(total_tokens, num_seqs));
+  uint32_t* ksf_tiles = reinterpret_cast<uint32_t*>(wsb + ws_ksf_off(ws_tokens, num_seqs));
   const int tq = p.plan.nq;
   const int max_items = total_tokens + num_seqs;
   p.w = w;
   p.cu_seqlens = cu_seqlens;
-  p.cu_keys = kpool_size > 1 ? cu_pools : cu_seqlens;
+  p.cu_keys = kpool_size > 1 ? cu_pools : (cu_k ? cu_k : cu_seqlens);
+  p.cu_seqlens_k = cu_k;
   p.out_idx = topk_idx;
   p.out_score = topk_score;
   p.out_len = topk_len;
@@ -350,13 +359,14 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   p.out_width = dsa_idx_output_width(index_topk, kpool_size, flags);
   p.fault_inject = g_fault_inject;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_build_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, tq, kpool_size,
-                                        items, doc_prefix, tile_base, hdr, max_items, st);
+  cudaError_t e = launch_build_worklist(cu_seqlens, cu_k, num_seqs, total_tokens, total_k, max_seqlen,
+                                        max_seqlen_k, tq, kpool_size, items, doc_prefix, tile_base, hdr,
+                                        max_items, st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   if (total_tokens == 0) return DSA_OK;
   if (fp8) {
     e = launch_tiled_kscales(k_scale, krows, p.cu_keys, tile_base, num_seqs,
-                             ws_ksf_tiles(total_tokens, num_seqs), ksf_tiles, di.sm_count, st);
+                             ws_ksf_tiles(ws_tokens, num_seqs), ksf_tiles, di.sm_count, st);
     if (e != cudaSuccess) return cuda_fail(e, "key-scale layout launch");
   }
   int grid = di.sm_count;
@@ -365,6 +375,35 @@ dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const voi
   e = launch_score_topk(p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "score_topk launch");
   return DSA_OK;
+}
+
+}  // namespace
+
+dsa_status_t dsa_idx_score_topk(const void* q, const uint8_t* q_scale, const void* k,
+                                const uint8_t* k_scale, const void* w, dsa_dtype_t w_dtype,
+                                float sm_scale, const int32_t* cu_seqlens, int num_seqs,
+                                int total_tokens, int max_seqlen, int n_heads, int head_dim,
+                                int index_topk, dsa_precision_t prec, int flags, int kpool_size,
+                                const int32_t* cu_pools, int32_t* topk_idx, float* topk_score,
+                                int32_t* topk_len, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  return score_topk_impl(q, q_scale, k, k_scale, w, w_dtype, sm_scale, cu_seqlens, nullptr, num_seqs,
+                         total_tokens, total_tokens, max_seqlen, max_seqlen, n_heads, head_dim, index_topk,
+                         prec, flags, kpool_size, cu_pools, topk_idx, topk_score, topk_len, ws, ws_bytes,
+                         stream);
+}
+
+dsa_status_t dsa_idx_score_topk_kv(const void* q, const uint8_t* q_scale, const void* k,
+                                   const uint8_t* k_scale, const void* w, dsa_dtype_t w_dtype,
+                                   float sm_scale, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k,
+                                   int max_seqlen_q, int max_seqlen_k, int n_heads, int head_dim,
+                                   int index_topk, dsa_precision_t prec, int flags, int32_t* topk_idx,
+                                   float* topk_score, int32_t* topk_len, void* ws, size_t ws_bytes,
+                                   dsa_stream_t stream) {
+  if (!cu_seqlens_k) return fail(DSA_ERR_INVALID_ARG, "cu_seqlens_k is NULL");
+  return score_topk_impl(q, q_scale, k, k_scale, w, w_dtype, sm_scale, cu_seqlens_q, cu_seqlens_k, num_seqs,
+                         total_q, total_k, max_seqlen_q, max_seqlen_k, n_heads, head_dim, index_topk, prec,
+                         flags, 1, nullptr, topk_idx, topk_score, topk_len, ws, ws_bytes, stream);
 }
 
 dsa_status_t dsa_idx_read_status(const void* ws, dsa_stream_t stream, dsa_status_t* out) {

@@ -69,7 +69,8 @@ struct ScoreParams {
   ScorePlan plan;
   const void* w;
   const int32_t* cu_seqlens;
-  const int32_t* cu_keys;   // cu_seqlens, or cu_pools in pool mode
+  const int32_t* cu_keys;   // first key row of each document: cu_seqlens_k, or cu_pools in pool mode
+  const int32_t* cu_seqlens_k;   // keys per document when they outnumber its queries, else null
   int32_t* out_idx;
   float* out_score;
   int32_t* out_len;

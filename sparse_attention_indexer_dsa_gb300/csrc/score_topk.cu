@@ -63,10 +63,13 @@ __device__ long long g_trace[16][256];
 constexpr int kWLThreads = 1024;
 constexpr int kWLMaxBins = 1025;
 
+// With cu_k (keys per document outnumbering its queries), document d's queries
+// are its last cu[d+1]-cu[d] tokens: query i sits at position off_d + i,
+// off_d = (cu_k[d+1]-cu_k[d]) - (cu[d+1]-cu[d]), and sees keys 0 .. off_d + i.
 __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
-    const int32_t* __restrict__ cu, int num_seqs, int total_tokens, int max_seqlen, int tq,
-    int pool, int2* __restrict__ items, int* __restrict__ doc_prefix, int* __restrict__ tile_base,
-    int* __restrict__ hdr, int max_items) {
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k, int num_seqs, int total_tokens,
+    int total_k, int max_seqlen, int max_seqlen_k, int tq, int pool, int2* __restrict__ items,
+    int* __restrict__ doc_prefix, int* __restrict__ tile_base, int* __restrict__ hdr, int max_items) {
   __shared__ int hist[kWLMaxBins];
   __shared__ int s_bad;
   __shared__ int s_total;
@@ -78,12 +81,17 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
   }
   for (int b = tid; b < kWLMaxBins; b += kWLThreads) hist[b] = 0;
   __syncthreads();
-  // validate cu_seqlens
+  // validate cu_seqlens (and cu_seqlens_k: at least as many keys as queries per document)
   for (int d = tid; d < num_seqs; d += kWLThreads) {
     const int a = cu[d], b = cu[d + 1];
     if (b < a || b - a > max_seqlen) s_bad = 1;
+    if (cu_k) {
+      const int ak = cu_k[d], bk = cu_k[d + 1];
+      if (bk < ak || bk - ak > max_seqlen_k || bk - ak < b - a) s_bad = 1;
+    }
   }
   if (tid == 0 && (cu[0] != 0 || cu[num_seqs] != total_tokens)) s_bad = 1;
+  if (tid == 0 && cu_k && (cu_k[0] != 0 || cu_k[num_seqs] != total_k)) s_bad = 1;
   __syncthreads();
   if (s_bad) {
     if (tid == 0) set_status(hdr, DSA_DEV_ERR_INVALID_ARG);
@@ -122,8 +130,8 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
     const int d = base + tid;
     int v = 0;
     if (d < num_seqs) {
-      const int L = cu[d + 1] - cu[d];
-      v = ((pool > 1 ? L / pool : L) + kTileKeys - 1) / kTileKeys;
+      const int S = cu_k ? cu_k[d + 1] - cu_k[d] : cu[d + 1] - cu[d];   // keys of the document
+      v = ((pool > 1 ? S / pool : S) + kTileKeys - 1) / kTileKeys;
     }
     int x = v;
     for (int o = 1; o < 32; o <<= 1) {
@@ -154,9 +162,10 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
   };
   auto tiles_of = [&](int d, int blk) {
     const int L = cu[d + 1] - cu[d];
+    const int off = cu_k ? (cu_k[d + 1] - cu_k[d]) - L : 0;
     int t_end = (blk + 1) * tq;
     if (t_end > L) t_end = L;
-    const int nk = pool > 1 ? t_end / pool : t_end;
+    const int nk = pool > 1 ? t_end / pool : off + t_end;
     int nt = (nk + kTileKeys - 1) / kTileKeys;
     return nt < kWLMaxBins - 1 ? nt : kWLMaxBins - 1;
   };
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(128) build_tiled_kscales_kernel(
 // helpers of the fused kernel
 // ----------------------------------------------------------------------------
 struct Item {
-  int doc, t0, L, qrow0, krow0, ntiles, ktile0;
+  int doc, t0, L, off, qrow0, krow0, ntiles, ktile0;   // off: position of the document's first query
 };
 
 __device__ __forceinline__ int item_index(int r, int nitems) {
@@ -226,9 +235,10 @@ __device__ __forceinline__ Item load_item(const ScoreParams& p, int i) {
   m.L = p.cu_seqlens[m.doc + 1] - a;
   m.qrow0 = (a + m.t0) * p.plan.n_heads;
   m.krow0 = p.cu_keys[m.doc];
+  m.off = p.cu_seqlens_k ? (p.cu_seqlens_k[m.doc + 1] - p.cu_seqlens_k[m.doc]) - m.L : 0;
   int t_end = m.t0 + p.plan.nq;
   if (t_end > m.L) t_end = m.L;
-  const int nk = p.pool > 1 ? t_end / p.pool : t_end;
+  const int nk = p.pool > 1 ? t_end / p.pool : m.off + t_end;
   m.ntiles = (nk + kTileKeys - 1) / kTileKeys;
   m.ktile0 = p.ksf_tiles ? p.tile_base[m.doc] : 0;
   return m;
@@ -880,7 +890,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         count[qi] = 0;
         tau[qi] = 0u;
         const int tq = qbase + qi;
-        vis_lim[qi] = tq >= m.L ? -1 : (p.pool > 1 ? (tq + 1) / p.pool - 1 : tq);
+        vis_lim[qi] = tq >= m.L ? -1 : (p.pool > 1 ? (tq + 1) / p.pool - 1 : m.off + tq);
       }
       named_bar_sync(bar_id, 128);
       // fragment path: this thread's 16 head weights stay in registers for the item
@@ -1268,11 +1278,13 @@ __global__ void __launch_bounds__(128, 1) debug_mma_tile_kernel(const __grid_con
 // ----------------------------------------------------------------------------
 // launchers (called from api.cu)
 // ----------------------------------------------------------------------------
-cudaError_t launch_build_worklist(const int32_t* cu, int num_seqs, int total_tokens, int max_seqlen,
-                                  int tq, int pool, int2* items, int* doc_prefix, int* tile_base,
-                                  int* hdr, int max_items, cudaStream_t stream) {
-  build_worklist_kernel<<<1, kWLThreads, 0, stream>>>(cu, num_seqs, total_tokens, max_seqlen, tq,
-                                                      pool, items, doc_prefix, tile_base, hdr, max_items);
+cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, int num_seqs, int total_tokens,
+                                  int total_k, int max_seqlen, int max_seqlen_k, int tq, int pool,
+                                  int2* items, int* doc_prefix, int* tile_base, int* hdr, int max_items,
+                                  cudaStream_t stream) {
+  build_worklist_kernel<<<1, kWLThreads, 0, stream>>>(cu, cu_k, num_seqs, total_tokens, total_k, max_seqlen,
+                                                      max_seqlen_k, tq, pool, items, doc_prefix, tile_base,
+                                                      hdr, max_items);
   return cudaGetLastError();
 }
 

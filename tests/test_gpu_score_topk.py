@@ -9,6 +9,7 @@ import torch
 
 import oracle.dsa_oracle as O
 import sparse_attention_indexer_dsa_gb300 as dsa
+from sparse_attention_indexer_dsa_gb300 import _abi
 from sparse_attention_indexer_dsa_gb300 import workloads as W
 from tests.gpu_util import bf16_dev, dev, host
 from tests.parity import REL_BF16, REL_MXFP8, compare_topk
@@ -264,3 +265,81 @@ def test_host_argument_errors():
     with pytest.raises(dsa.DsaError, match="UNSUPPORTED"):
         dsa.score_topk(t.view(1, 16), None, t.view(1, 16), None, torch.zeros(1, 3, device="cuda"),
                        dev(np.array([0, 1], np.int32)), 1, 3, 1, "bf16")
+
+
+# ---------------------------------------------------------------- global causal offsets
+
+def _run_kv(q_op, q_sc, k_op, k_sc, w, lens_q, lens_k, H, k, prec, sm_scale=1.0):
+    cuq = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cuk = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    idx, sc, ln = dsa.score_topk_kv(q_op, q_sc, k_op, k_sc, w, dev(cuq), dev(cuk), max(max(lens_q), 1),
+                                    max(lens_k), H, k, prec, sm_scale=sm_scale)
+    torch.cuda.synchronize()
+    return host(idx), host(sc), host(ln), cuq, cuk
+
+
+KV_CASES = [
+    # lens_q, lens_k, H, k, prec
+    ([64, 300, 1, 0], [700, 300, 130, 5], 64, 256, "bf16"),
+    ([64, 300, 1, 0], [700, 300, 130, 5], 64, 256, "mxfp8"),
+    ([40, 200], [2500, 900], 64, 2048, "mxfp8"),
+    ([3, 129, 17], [3, 400, 1000], 16, 100, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", KV_CASES, ids=[str(i) for i in range(len(KV_CASES))])
+def test_kv_offsets_random(case):
+    """Queries that are the last T_d tokens of S_d keys ([P1] review finding
+    2, global causal offsets), BF16 and MXFP8, including T_d = S_d, T_d = 1
+    and T_d = 0."""
+    lens_q, lens_k, H, k, prec = case
+    D = 128
+    Tq, Tk = sum(lens_q), sum(lens_k)
+    rng = np.random.default_rng(101 + H + k)
+    w = (rng.standard_normal((Tq, H)) * 0.2).astype(np.float32)
+    if prec == "bf16":
+        qb = W.random_bf16_bits(rng, (Tq * H, D))
+        kb = W.random_bf16_bits(rng, (Tk, D))
+        args = (bf16_dev(qb), None, bf16_dev(kb), None)
+        qd, kd, rel = O.bf16_bits_to_float(qb), O.bf16_bits_to_float(kb), REL_BF16
+    else:
+        qc, qs, qd = O.quantize_mxfp8(rng.standard_normal((Tq * H, D)))
+        kc, ks, kd = O.quantize_mxfp8(rng.standard_normal((Tk, D)))
+        args = (dev(qc), dev(qs), dev(kc), dev(ks))
+        rel = REL_MXFP8
+    g_idx, g_sc, g_ln, cuq, cuk = _run_kv(*args, dev(w), lens_q, lens_k, H, k, prec, sm_scale=0.5)
+    ref = O.indexer_topk(qd.reshape(Tq, H, D), kd, w.astype(np.float64), cuq, k, sm_scale=0.5, with_scale=True,
+                         cu_seqlens_k=cuk)
+    compare_topk(g_idx, g_sc, g_ln, ref, rel)
+
+
+def test_kv_offsets_integer_exact():
+    """Integer scores (ties everywhere) with offsets: bit-exact."""
+    rng = np.random.default_rng(111)
+    lens_q, lens_k, H, D, k = [50, 7, 260], [1800, 7, 300], 64, 128, 512
+    Tq, Tk = sum(lens_q), sum(lens_k)
+    q = rng.integers(-3, 4, (Tq, H, D)).astype(np.float64)
+    kk = rng.integers(-3, 4, (Tk, D)).astype(np.float64)
+    w = rng.integers(-2, 3, (Tq, H)).astype(np.float32)
+    qc, qs, _ = O.quantize_mxfp8(q.reshape(Tq * H, D))
+    kc, ks, _ = O.quantize_mxfp8(kk)
+    g_idx, g_sc, g_ln, cuq, cuk = _run_kv(dev(qc), dev(qs), dev(kc), dev(ks), dev(w), lens_q, lens_k, H, k, "mxfp8")
+    ref = O.indexer_topk(q, kk, w.astype(np.float64), cuq, k, cu_seqlens_k=cuk)
+    np.testing.assert_array_equal(g_ln, ref["len"])
+    np.testing.assert_array_equal(g_idx, ref["idx"])
+    np.testing.assert_array_equal(g_sc, ref["score"].astype(np.float32))
+
+
+def test_kv_more_queries_than_keys_sets_status():
+    """T_d > S_d is caught on the device: DSA_ERR_INVALID_ARG in the status word."""
+    H, D, k = 16, 128, 8
+    lens_q, lens_k = [10, 5], [10, 4]
+    Tq, Tk = sum(lens_q), sum(lens_k)
+    qb = torch.zeros((Tq * H, D), dtype=torch.bfloat16, device="cuda")
+    kb = torch.zeros((Tk, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones((Tq, H), dtype=torch.float32, device="cuda")
+    cuq = dev(np.array([0, 10, 15], np.int32))
+    cuk = dev(np.array([0, 10, 14], np.int32))
+    ws = dsa.workspace(max(Tq, Tk), 2, 10, H, D, k, 1, "bf16", qb.device)
+    dsa.score_topk_kv(qb, None, kb, None, w, cuq, cuk, 10, 10, H, k, "bf16", ws=ws)
+    assert dsa.read_status(ws) == _abi.DSA_ERR_INVALID_ARG
