@@ -418,6 +418,47 @@ def kpool_compress(k, gate, slot_bias, cu_seqlens, pool_size: int):
     return kbar, np.array(cu_pools, dtype=np.int64)
 
 
+def compressed_topk(q_op, kc_op, w, cu_seqlens, cu_comp, index_topk: int, ratio: int,
+                    sm_scale: float = 1.0, rows: Optional[Sequence[int]] = None, order: str = "index",
+                    with_scale: bool = False):
+    """Top-k over compressed keys ([P2] "[DeepSeek-V4] Add compact BF16 and
+    MXFP8 DSA indexer support": the indexer's `ratio`).  Compressed key c of
+    a document stands for its tokens c*ratio .. c*ratio + ratio - 1 and,
+    like a complete KPool pool, is visible to the query at local position p
+    once complete: c < (p+1) // ratio.  Each query keeps the best
+    min(index_topk, visible) compressed keys (score desc, index asc); indices
+    are local to the document's compressed keys (no expansion to tokens);
+    -1 / -inf padding; len = number kept.  kc_op [total compressed, D],
+    cu_comp [B+1] its per-document prefix (at least floor(L/ratio) keys per
+    document; extra keys are never visible).
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cc = np.asarray(cu_comp, dtype=np.int64)
+    T = int(cu[-1])
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    doc_of = np.searchsorted(cu, rows, side="right") - 1
+    R = len(rows)
+    out_idx = np.full((R, index_topk), -1, dtype=np.int64)
+    out_sc = np.full((R, index_topk), -np.inf)
+    out_len = np.zeros(R, dtype=np.int64)
+    all_scores, all_scales = [], []
+    for r, (t, d) in enumerate(zip(rows, doc_of)):
+        p = t - cu[d]
+        nvis = (p + 1) // ratio
+        kv = kc_op[cc[d]:cc[d] + nvis]
+        s = indexer_scores(q_op[t], kv, w[t], sm_scale)
+        chosen = select_topk(s, index_topk)
+        out_idx[r], out_sc[r], out_len[r] = _finish_row(chosen, s, index_topk, order)
+        if with_scale:
+            all_scores.append(s)
+            all_scales.append(error_scale(q_op[t], kv, w[t], sm_scale))
+    res = dict(rows=rows, idx=out_idx, score=out_sc, len=out_len)
+    if with_scale:
+        res["all_scores"] = all_scores
+        res["all_scales"] = all_scales
+    return res
+
+
 def kpool_topk(q_op, kbar_op, w, cu_seqlens, cu_pools, index_topk: int, pool_size: int,
                always_select_tail: bool = True, sm_scale: float = 1.0,
                rows: Optional[Sequence[int]] = None, order: str = "index",

@@ -411,6 +411,57 @@ def test_global_offsets_brute_force():
             row += 1
 
 
+# ----------------------------------------------------------------- compressed keys
+
+def test_compressed_ratio_one_is_the_plain_indexer():
+    rng = np.random.default_rng(21)
+    lens = [9, 4]
+    q = rng.standard_normal((13, 2, 8))
+    k = rng.standard_normal((13, 8))
+    w = rng.standard_normal((13, 2))
+    cu = [0, 9, 13]
+    a = O.compressed_topk(q, k, w, cu, cu, 5, 1)
+    b = O.indexer_topk(q, k, w, cu, 5)
+    for key in ("idx", "score", "len"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_compressed_selection_matches_kpool_pools():
+    """Given pooled keys, the compressed selection of index_topk / P keys is
+    exactly the set of pools KPool expands (its tokens / P, tail excluded)."""
+    rng = np.random.default_rng(22)
+    lens, P, kk = [23, 10], 4, 12
+    T = sum(lens)
+    q = rng.integers(-2, 3, (T, 2, 8)).astype(np.float64)
+    k = rng.standard_normal((T, 8))
+    w = rng.integers(-2, 3, (T, 2)).astype(np.float64)
+    cu = np.array([0, 23, 33])
+    kbar, cp = O.kpool_compress(k, rng.standard_normal(T), rng.standard_normal(P), cu, P)
+    c = O.compressed_topk(q, kbar, w, cu, cp, kk // P, P)
+    kp = O.kpool_topk(q, kbar, w, cu, cp, kk, P, always_select_tail=False)
+    for r in range(T):
+        n = c["len"][r]
+        assert kp["len"][r] == n * P
+        np.testing.assert_array_equal(kp["idx"][r][:n * P:P] // P, c["idx"][r][:n])
+        np.testing.assert_array_equal(kp["score"][r][:n * P:P], c["score"][r][:n])
+
+
+def test_compressed_visibility_brute_force():
+    rng = np.random.default_rng(23)
+    ratio, L = 3, 11
+    q = rng.standard_normal((L, 2, 4))
+    kc = rng.standard_normal((4, 4))     # ceil(11 / 3): the last one is never complete
+    w = rng.standard_normal((L, 2))
+    r = O.compressed_topk(q, kc, w, [0, L], [0, 4], 2, ratio)
+    for t in range(L):
+        nvis = sum(1 for c in range(4) if c * ratio + ratio - 1 <= t)
+        sc = _brute_scores(q[t], kc[:nvis], w[t], 1.0)
+        best = sorted(sorted(range(nvis), key=lambda s_: (-sc[s_], s_))[:2])
+        assert r["len"][t] == len(best)
+        np.testing.assert_array_equal(r["idx"][t][:len(best)], best)
+        assert (r["idx"][t][len(best):] == -1).all()
+
+
 # ----------------------------------------------------------------- KPool
 
 def test_kpool_single_slot_reduces_to_plain_indexer():
