@@ -83,6 +83,10 @@ typedef enum { DSA_MX_SCALE_NOSAT = 0, DSA_MX_SCALE_FLOOR = 1 } dsa_mx_scale_rul
 #define DSA_FLAG_DETERMINISTIC 0x1   /* [P2] deterministic Top-K tie break; always honoured */
 #define DSA_FLAG_SORT_BY_SCORE 0x2   /* rows in (score desc, index asc) order instead of index asc */
 #define DSA_FLAG_KPOOL_TAIL 0x4      /* [P3] always_select_tail: append the query's incomplete pool */
+/* [P2] compressed keys: kpool_size is the indexer's `ratio` (2..64); k holds
+ * caller-computed compressed keys, cu_pools their per-document prefix; each
+ * query keeps index_topk compressed keys, indices not expanded to tokens. */
+#define DSA_FLAG_COMPRESSED_KEYS 0x8
 
 /* Library version (major*10000 + minor*100 + patch). */
 int dsa_idx_version(void);
@@ -179,12 +183,21 @@ dsa_status_t dsa_idx_kpool_compress(
  *               kpool_size, and index_topk / kpool_size pools are kept
  *   prec     BF16 (kind::f16) or MXFP8 (block-scaled kind::mxf8f6f4)
  *   flags    DSA_FLAG_* bits
- *   kpool_size  1 = plain keys; >1 = pool mode (cu_pools required)
+ *   kpool_size  1 = plain keys; >1 = pool mode (cu_pools required): KPool
+ *               pools of that size (2, 4 or 8), or with
+ *               DSA_FLAG_COMPRESSED_KEYS the compression ratio (2..64) of
+ *               caller-provided compressed keys.  Either way key c of a
+ *               document covers its tokens c*kpool_size .. +kpool_size-1
+ *               and is visible once complete; k has room for
+ *               total_tokens / kpool_size rows and document d's keys are
+ *               rows cu_pools[d] .. cu_pools[d+1]-1 (at least
+ *               floor(L_d / kpool_size) of them; more are never visible)
  *   topk_idx    device int32 [total_tokens, W] (W = dsa_idx_output_width):
  *               selected local indices in ascending order, then -1
  *               padding (DSA_FLAG_SORT_BY_SCORE is reserved and returns
- *               DSA_ERR_UNSUPPORTED).  Pool mode: the
- *               expanded tokens of the selected pools, then the tail tokens.
+ *               DSA_ERR_UNSUPPORTED).  KPool mode: the expanded tokens of
+ *               the selected pools, then the tail tokens.  Compressed keys:
+ *               the selected compressed-key indices (W = index_topk).
  *   topk_score  device fp32 [total_tokens, W] or NULL: the score of each
  *               entry (pooled score for pool tokens, +INF for tail tokens,
  *               -INF for padding)

@@ -14,7 +14,8 @@ from typing import Optional, Tuple
 import torch
 
 from . import _abi
-from ._abi import (DSA_FLAG_DETERMINISTIC, DSA_FLAG_KPOOL_TAIL, DSA_FLAG_SORT_BY_SCORE,  # noqa: F401
+from ._abi import (DSA_FLAG_COMPRESSED_KEYS, DSA_FLAG_DETERMINISTIC, DSA_FLAG_KPOOL_TAIL,  # noqa: F401
+                   DSA_FLAG_SORT_BY_SCORE,
                    DSA_PREC_BF16, DSA_PREC_MXFP8)
 
 __all__ = [
@@ -146,15 +147,22 @@ def score_topk(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: torch.
                k_scale: Optional[torch.Tensor], w: torch.Tensor, cu_seqlens: torch.Tensor,
                max_seqlen: int, n_heads: int, index_topk: int, prec="bf16", sm_scale: float = 1.0,
                kpool_size: int = 1, cu_pools: Optional[torch.Tensor] = None, tail: bool = True,
-               return_scores: bool = True, ws: Optional[torch.Tensor] = None, out=None):
+               return_scores: bool = True, ws: Optional[torch.Tensor] = None, out=None,
+               compressed: bool = False):
     """Fused score + top-k (dsa_idx_score_topk).
 
     q_op [T*H, D] (bf16 or E4M3 codes), k_op [rows, D], w [T, H] fp32/bf16.
+    kpool_size > 1: KPool pools of that size, or with compressed=True the
+    compression ratio of caller-provided compressed keys (cu_pools = their
+    per-document prefix; indices are reported per compressed key).
     Returns (idx int32 [T, W], scores fp32 [T, W] or None, lens int32 [T])."""
     T = w.shape[0]
     D = q_op.shape[-1]
     B = cu_seqlens.numel() - 1
-    flags = DSA_FLAG_DETERMINISTIC | (DSA_FLAG_KPOOL_TAIL if (kpool_size > 1 and tail) else 0)
+    if compressed:
+        flags = DSA_FLAG_DETERMINISTIC | DSA_FLAG_COMPRESSED_KEYS
+    else:
+        flags = DSA_FLAG_DETERMINISTIC | (DSA_FLAG_KPOOL_TAIL if (kpool_size > 1 and tail) else 0)
     W = _abi.load().dsa_idx_output_width(index_topk, kpool_size, flags)
     if out is None:
         idx = torch.empty((T, W), dtype=torch.int32, device=q_op.device)

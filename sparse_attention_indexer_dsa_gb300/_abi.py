@@ -30,6 +30,7 @@ DSA_MX_SCALE_FLOOR = 1
 DSA_FLAG_DETERMINISTIC = 0x1
 DSA_FLAG_SORT_BY_SCORE = 0x2
 DSA_FLAG_KPOOL_TAIL = 0x4
+DSA_FLAG_COMPRESSED_KEYS = 0x8
 
 _c_int, _c_i64, _c_f, _c_size, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 

@@ -172,6 +172,7 @@ size_t dsa_idx_workspace_size(int total_tokens, int num_seqs, int max_seqlen, in
 }
 
 int dsa_idx_output_width(int index_topk, int kpool_size, int flags) {
+  if (flags & DSA_FLAG_COMPRESSED_KEYS) return index_topk;
   if (kpool_size > 1 && (flags & DSA_FLAG_KPOOL_TAIL)) return index_topk + kpool_size - 1;
   return index_topk;
 }
@@ -297,18 +298,24 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
     return fail(DSA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   }
   if (w_dtype != DSA_DTYPE_F32 && w_dtype != DSA_DTYPE_BF16) return fail(DSA_ERR_INVALID_ARG, "w_dtype");
-  if (flags & ~(DSA_FLAG_DETERMINISTIC | DSA_FLAG_SORT_BY_SCORE | DSA_FLAG_KPOOL_TAIL))
+  if (flags & ~(DSA_FLAG_DETERMINISTIC | DSA_FLAG_SORT_BY_SCORE | DSA_FLAG_KPOOL_TAIL | DSA_FLAG_COMPRESSED_KEYS))
     return fail(DSA_ERR_INVALID_ARG, "unknown flag bits");
   if (flags & DSA_FLAG_SORT_BY_SCORE) return fail(DSA_ERR_UNSUPPORTED, "DSA_FLAG_SORT_BY_SCORE is not implemented");
+  const bool compressed = (flags & DSA_FLAG_COMPRESSED_KEYS) != 0;
   if (kpool_size < 1) return fail(DSA_ERR_INVALID_ARG, "kpool_size");
-  if (kpool_size > 1) {
+  if (compressed) {
+    if (kpool_size < 2 || kpool_size > 64) return fail(DSA_ERR_UNSUPPORTED, "compression ratio must be 2..64");
+    if (!cu_pools) return fail(DSA_ERR_INVALID_ARG, "compressed keys need cu_pools");
+    if (flags & DSA_FLAG_KPOOL_TAIL) return fail(DSA_ERR_INVALID_ARG, "DSA_FLAG_KPOOL_TAIL applies to KPool only");
+  } else if (kpool_size > 1) {
     if (kpool_size != 2 && kpool_size != 4 && kpool_size != 8) return fail(DSA_ERR_UNSUPPORTED, "kpool_size must be 1, 2, 4 or 8");
     if (!cu_pools) return fail(DSA_ERR_INVALID_ARG, "pool mode needs cu_pools");
     if (index_topk % kpool_size != 0) return fail(DSA_ERR_INVALID_ARG, "index_topk must be a multiple of kpool_size");
   }
-  if (index_topk < 1 || index_topk > 2048 * (kpool_size > 1 ? kpool_size : 1))
+  const int expand = kpool_size > 1 && !compressed ? kpool_size : 1;   // tokens per selected key in the output
+  if (index_topk < 1 || index_topk > 2048 * expand)
     return fail(DSA_ERR_UNSUPPORTED, "index_topk must be in [1, 2048] (pools)");
-  const int keep = index_topk / kpool_size;
+  const int keep = index_topk / expand;
   if (keep < 1) return fail(DSA_ERR_INVALID_ARG, "index_topk / kpool_size must be >= 1");
   if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
   const bool mxw = prec == DSA_PREC_MXFP8;
@@ -355,13 +362,14 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   p.sm_scale = sm_scale;
   p.w_bf16 = w_dtype == DSA_DTYPE_BF16;
   p.pool = kpool_size;
-  p.tail = (kpool_size > 1 && (flags & DSA_FLAG_KPOOL_TAIL)) ? 1 : 0;
+  p.expand = expand > 1 ? 1 : 0;
+  p.tail = (expand > 1 && (flags & DSA_FLAG_KPOOL_TAIL)) ? 1 : 0;
   p.out_width = dsa_idx_output_width(index_topk, kpool_size, flags);
   p.fault_inject = g_fault_inject;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_build_worklist(cu_seqlens, cu_k, num_seqs, total_tokens, total_k, max_seqlen,
-                                        max_seqlen_k, tq, kpool_size, items, doc_prefix, tile_base, hdr,
-                                        max_items, st);
+  cudaError_t e = launch_build_worklist(cu_seqlens, cu_k, compressed ? cu_pools : nullptr, num_seqs, total_tokens,
+                                        total_k, max_seqlen, max_seqlen_k, tq, kpool_size, items, doc_prefix,
+                                        tile_base, hdr, max_items, st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   if (total_tokens == 0) return DSA_OK;
   if (fp8) {

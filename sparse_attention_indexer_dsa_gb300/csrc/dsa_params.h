@@ -39,7 +39,8 @@ cudaError_t launch_quantize_mxfp8(const void* x, int in_bf16, int64_t nblocks, i
 cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const float* bias,
                          const int32_t* cu, int num_seqs, int total_tokens, int D, int P,
                          uint16_t* out, int32_t* cu_pools, int sm_count, cudaStream_t stream);
-cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, int num_seqs, int total_tokens,
+cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, const int32_t* cu_comp, int num_seqs,
+                                  int total_tokens,
                                   int total_k, int max_seqlen, int max_seqlen_k, int tq, int pool,
                                   int2* items, int* doc_prefix, int* tile_base, int* hdr, int max_items,
                                   cudaStream_t stream);

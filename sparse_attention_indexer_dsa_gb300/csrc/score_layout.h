@@ -81,7 +81,8 @@ struct ScoreParams {
   unsigned long long timeout_ns;
   float sm_scale;
   int w_bf16;
-  int pool;                 // 1 = plain keys
+  int pool;                 // 1 = plain keys, else tokens per (pooled or compressed) key
+  int expand;               // 1: expand each selected pool to its tokens (KPool); 0: report key indices
   int tail;                 // append the query's incomplete pool (pool mode)
   int out_width;
   int fault_inject;         // test hook: 1 = the first K stage is never loaded

@@ -67,7 +67,8 @@ constexpr int kWLMaxBins = 1025;
 // are its last cu[d+1]-cu[d] tokens: query i sits at position off_d + i,
 // off_d = (cu_k[d+1]-cu_k[d]) - (cu[d+1]-cu[d]), and sees keys 0 .. off_d + i.
 __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
-    const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k, int num_seqs, int total_tokens,
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ cu_comp,
+    int num_seqs, int total_tokens,
     int total_k, int max_seqlen, int max_seqlen_k, int tq, int pool, int2* __restrict__ items,
     int* __restrict__ doc_prefix, int* __restrict__ tile_base, int* __restrict__ hdr, int max_items) {
   __shared__ int hist[kWLMaxBins];
@@ -92,6 +93,12 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
   }
   if (tid == 0 && (cu[0] != 0 || cu[num_seqs] != total_tokens)) s_bad = 1;
   if (tid == 0 && cu_k && (cu_k[0] != 0 || cu_k[num_seqs] != total_k)) s_bad = 1;
+  // caller-provided compressed keys: room for every complete group, within total_tokens / pool rows
+  if (cu_comp) {
+    for (int d = tid; d < num_seqs; d += kWLThreads)
+      if (cu_comp[d + 1] - cu_comp[d] < (cu[d + 1] - cu[d]) / pool) s_bad = 1;
+    if (tid == 0 && (cu_comp[0] < 0 || cu_comp[num_seqs] > total_tokens / pool)) s_bad = 1;
+  }
   __syncthreads();
   if (s_bad) {
     if (tid == 0) set_status(hdr, DSA_DEV_ERR_INVALID_ARG);
@@ -1138,7 +1145,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         const int n = count[qi];
         const uint32_t* ck = ckey_base + qi * C;
         const uint16_t* ci = cidx_base + qi * C;
-        if (p.pool > 1) {
+        if (p.expand) {
           const int P = p.pool;
           const int ntail = p.tail ? (tq + 1) % P : 0;
           const int tail0 = P * ((tq + 1) / P);
@@ -1278,11 +1285,11 @@ __global__ void __launch_bounds__(128, 1) debug_mma_tile_kernel(const __grid_con
 // ----------------------------------------------------------------------------
 // launchers (called from api.cu)
 // ----------------------------------------------------------------------------
-cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, int num_seqs, int total_tokens,
-                                  int total_k, int max_seqlen, int max_seqlen_k, int tq, int pool,
-                                  int2* items, int* doc_prefix, int* tile_base, int* hdr, int max_items,
-                                  cudaStream_t stream) {
-  build_worklist_kernel<<<1, kWLThreads, 0, stream>>>(cu, cu_k, num_seqs, total_tokens, total_k, max_seqlen,
+cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, const int32_t* cu_comp, int num_seqs,
+                                  int total_tokens, int total_k, int max_seqlen, int max_seqlen_k, int tq,
+                                  int pool, int2* items, int* doc_prefix, int* tile_base, int* hdr,
+                                  int max_items, cudaStream_t stream) {
+  build_worklist_kernel<<<1, kWLThreads, 0, stream>>>(cu, cu_k, cu_comp, num_seqs, total_tokens, total_k, max_seqlen,
                                                       max_seqlen_k, tq, pool, items, doc_prefix, tile_base,
                                                       hdr, max_items);
   return cudaGetLastError();

@@ -343,3 +343,63 @@ def test_kv_more_queries_than_keys_sets_status():
     ws = dsa.workspace(max(Tq, Tk), 2, 10, H, D, k, 1, "bf16", qb.device)
     dsa.score_topk_kv(qb, None, kb, None, w, cuq, cuk, 10, 10, H, k, "bf16", ws=ws)
     assert dsa.read_status(ws) == _abi.DSA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- compressed keys (ratio > 1)
+
+COMP_CASES = [
+    # lens, ratio, H, k, prec
+    ([1500, 37, 400], 4, 64, 256, "bf16"),
+    ([1500, 37, 400], 4, 64, 256, "mxfp8"),
+    ([4000, 900], 2, 64, 2048, "mxfp8"),
+    ([2000, 3, 700], 16, 32, 50, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", COMP_CASES, ids=[str(i) for i in range(len(COMP_CASES))])
+def test_compressed_keys_random(case):
+    """Caller-provided compressed keys ([P2], the indexer's ratio): key c of a
+    document covers its tokens c*ratio .. c*ratio + ratio - 1 and is visible
+    once complete; indices are per compressed key."""
+    lens, ratio, H, k, prec = case
+    D = 128
+    T = sum(lens)
+    ncomp = [L // ratio for L in lens]
+    cc = np.concatenate([[0], np.cumsum(ncomp)]).astype(np.int32)
+    rng = np.random.default_rng(121 + ratio + k)
+    w = (rng.standard_normal((T, H)) * 0.2).astype(np.float32)
+    rows_k = max(T // ratio, 1)     # the documented room: total_tokens / ratio rows
+    if prec == "bf16":
+        qb = W.random_bf16_bits(rng, (T * H, D))
+        kb = W.random_bf16_bits(rng, (rows_k, D))
+        args = (bf16_dev(qb), None, bf16_dev(kb), None)
+        qd, kd, rel = O.bf16_bits_to_float(qb), O.bf16_bits_to_float(kb), REL_BF16
+    else:
+        qc, qs, qd = O.quantize_mxfp8(rng.standard_normal((T * H, D)))
+        kc, ks, kd = O.quantize_mxfp8(rng.standard_normal((rows_k, D)))
+        args = (dev(qc), dev(qs), dev(kc), dev(ks))
+        rel = REL_MXFP8
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    idx, sc, ln = dsa.score_topk(*args, dev(w), dev(cu), max(lens), H, k, prec, sm_scale=0.5, kpool_size=ratio,
+                                 cu_pools=dev(cc), compressed=True)
+    torch.cuda.synchronize()
+    ref = O.compressed_topk(qd.reshape(T, H, D), kd, w.astype(np.float64), cu, cc, k, ratio, sm_scale=0.5,
+                            with_scale=True)
+    compare_topk(host(idx), host(sc), host(ln), ref, rel)
+
+
+def test_compressed_keys_too_few_rows_sets_status():
+    """A document with fewer compressed keys than complete groups is caught on
+    the device (DSA_ERR_INVALID_ARG in the status word)."""
+    H, D, k, ratio = 16, 128, 8, 4
+    lens = [40, 12]
+    T = sum(lens)
+    qb = torch.zeros((T * H, D), dtype=torch.bfloat16, device="cuda")
+    kb = torch.zeros((T // ratio, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones((T, H), dtype=torch.float32, device="cuda")
+    cu = dev(np.array([0, 40, 52], np.int32))
+    cc = dev(np.array([0, 9, 12], np.int32))     # document 0 has 10 complete groups
+    ws = dsa.workspace(T, 2, 40, H, D, k, ratio, "bf16", qb.device)
+    dsa.score_topk(qb, None, kb, None, w, cu, 40, H, k, "bf16", kpool_size=ratio, cu_pools=cc, compressed=True,
+                   ws=ws)
+    assert dsa.read_status(ws) == _abi.DSA_ERR_INVALID_ARG
