@@ -199,6 +199,27 @@ def quantize_mxfp8(x, rule: str = "nosat") -> Tuple[np.ndarray, np.ndarray, np.n
     return codes, sbytes, deq
 
 
+def quantize_fp8_rows(x, rule: str = "nosat") -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """FP8 with one UE8M0 scale per vector ([P1] "What does this PR do?": the
+    SM90 path's FP8 scoring with per-vector UE8M0 scales).  Each row of x
+    [..., D] gets the exponent mx_block_exponent(max |row|, rule), i.e. the
+    MXFP8 block rule applied to the whole row, and payload =
+    E4M3_RNE_sat(x / 2^e).  Returns (codes uint8 [..., D], scale bytes uint8
+    [...] = e + 127, dequantised float64 values payload * 2^e).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    xr = x.reshape(-1, D)
+    amax = np.abs(xr).max(axis=-1)
+    e = np.vectorize(lambda a: mx_block_exponent(float(a), rule), otypes=[np.int64])(amax)
+    scale = np.ldexp(1.0, e)[:, None]
+    payload = round_e4m3_sat(xr / scale)
+    deq = (payload * scale).reshape(x.shape)
+    codes = e4m3_encode(payload).reshape(x.shape)
+    sbytes = (e + UE8M0_BIAS).astype(np.uint8).reshape(x.shape[:-1])
+    return codes, sbytes, deq
+
+
 def dequantize_mxfp8(codes, scale_bytes) -> np.ndarray:
     """float64 value of MXFP8 data: e4m3_decode(code) * 2^(scale_byte - 127)."""
     codes = np.asarray(codes)
@@ -292,10 +313,14 @@ def preprocess(q, k, cu_seqlens, gamma=None, beta=None, eps: float = 1e-6,
 
 def scoring_operand(carrier, prec: str, rule: str = "nosat"):
     """Scoring operand from a carrier: "bf16" -> RNE to BF16 ([P1] finding 2);
-    "mxfp8" -> quantize_mxfp8 along the last axis.  Returns (values float64,
+    "mxfp8" -> quantize_mxfp8 along the last axis; "fp8" -> quantize_fp8_rows
+    (one scale per row).  Returns (values float64,
     codes or None, scale bytes or None)."""
     if prec == "bf16":
         return round_bf16(carrier), None, None
+    if prec == "fp8":
+        codes, sb, deq = quantize_fp8_rows(carrier, rule)
+        return deq, codes, sb
     codes, sb, deq = quantize_mxfp8(carrier, rule)
     return deq, codes, sb
 

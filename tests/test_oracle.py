@@ -411,6 +411,49 @@ def test_global_offsets_brute_force():
             row += 1
 
 
+# ----------------------------------------------------------------- FP8 with per-vector scales
+
+def test_fp8_rows_of_32_equal_the_mx_block_rule():
+    """A 32-element row is one MX block: the per-vector quantiser must agree
+    with the (separately pinned) MXFP8 quantiser code for code."""
+    x = np.random.default_rng(24).standard_normal((300, 32)) * np.exp(np.random.default_rng(25).uniform(-20, 20, (300, 1)))
+    c1, s1, d1 = O.quantize_fp8_rows(x)
+    c2, s2, d2 = O.quantize_mxfp8(x)
+    np.testing.assert_array_equal(c1, c2)
+    np.testing.assert_array_equal(s1, s2[:, 0])
+    np.testing.assert_array_equal(d1, d2)
+
+
+def test_fp8_rows_power_of_two_invariance_and_range():
+    rng = np.random.default_rng(26)
+    x = rng.standard_normal((50, 128))
+    c, sb, d = O.quantize_fp8_rows(x)
+    c8, sb8, d8 = O.quantize_fp8_rows(x * 2.0 ** 9)
+    np.testing.assert_array_equal(c8, c)
+    np.testing.assert_array_equal(sb8.astype(int), sb.astype(int) + 9)
+    amax = np.abs(x).max(axis=1)
+    scale = np.ldexp(1.0, sb.astype(int) - 127)
+    assert (amax <= 448 * scale).all() and (amax > 448 * scale / 2).all()   # the smallest such exponent
+    assert np.abs(d - x).max(axis=1).max() <= (scale * 2.0 ** 5).max()        # within half an E4M3 step
+
+
+def test_fp8_scale_folding_is_exact():
+    """The per-vector scales are positive powers of two and ReLU is positively
+    homogeneous, so scoring the dequantised operands equals scoring the raw
+    payloads with w_j * s_q[j] and the result times s_k, exactly."""
+    rng = np.random.default_rng(27)
+    q = rng.standard_normal((4, 32)) * 3
+    k = rng.standard_normal((9, 32))
+    w = rng.standard_normal(4)
+    qc, qs, qd = O.quantize_fp8_rows(q)
+    kc, ks, kd = O.quantize_fp8_rows(k)
+    direct = O.indexer_scores(qd, kd, w, 0.5)
+    sq = np.ldexp(1.0, qs.astype(int) - 127)
+    sk = np.ldexp(1.0, ks.astype(int) - 127)
+    folded = O.indexer_scores(O.e4m3_decode(qc), O.e4m3_decode(kc), w * sq, 0.5) * sk
+    np.testing.assert_array_equal(folded, direct)
+
+
 # ----------------------------------------------------------------- compressed keys
 
 def test_compressed_ratio_one_is_the_plain_indexer():
