@@ -70,13 +70,13 @@ def round_to_format(x, mant_bits: int, emin: int, max_finite: float = math.inf,
     The spacing of the format around |x| is 2^(floor(log2|x|) - mant_bits) for
     normal numbers and 2^(emin - mant_bits) below 2^emin; x / spacing is
     rounded half-to-even (np.rint) and scaled back.  Both scalings are exact
-    (powers of two).  Values beyond max_finite become +-inf, or +-max_finite
-    when `saturate`.
+    (powers of two); -0 stays -0.  Values beyond max_finite become +-inf, or
+    +-max_finite when `saturate`.
     """
     x = np.asarray(x, dtype=np.float64)
-    out = np.zeros_like(x)
     ax = np.abs(x)
     nz = ax > 0
+    out = np.where(nz, 0.0, x)          # a zero rounds to itself, sign included
     _, e2 = np.frexp(ax[nz])            # ax = m * 2^e2, m in [0.5, 1)
     exp = np.maximum(e2 - 1, emin)      # floor(log2|x|), clamped to subnormal range
     spacing = np.ldexp(1.0, exp - mant_bits)

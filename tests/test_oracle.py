@@ -70,6 +70,21 @@ def test_e4m3_codes_match_torch_and_round_trip():
     assert O.e4m3_decode([0x38])[0] == 1.0
 
 
+def test_signed_zero_survives_rounding_and_quantisation():
+    """-0 rounds to -0 in every format and quantises to the E4M3 code 0x80,
+    as torch's casts do."""
+    z = np.array([-0.0, 0.0])
+    for r in (O.round_bf16(z), O.round_fp32(z), O.round_e4m3_sat(z)):
+        assert np.signbit(r[0]) and not np.signbit(r[1])
+    ref = torch.tensor([-0.0, 0.0]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    row = np.zeros((1, 32))
+    row[0, 5] = -0.0
+    row[0, 6] = 1.5
+    np.testing.assert_array_equal(O.quantize_mxfp8(row)[0][0, 5:7], [ref[0], O.quantize_mxfp8(row)[0][0, 6]])
+    assert O.quantize_fp8_rows(row)[0][0, 5] == ref[0] == 0x80
+    assert O.e4m3_encode(O.round_e4m3_sat(z)).tolist() == ref.tolist()
+
+
 def test_bf16_bits_round_trip():
     rng = np.random.default_rng(3)
     bits = rng.integers(0, 2 ** 16, 5000).astype(np.uint16)
