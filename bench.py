@@ -37,10 +37,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 
 
-def describe(wl):
+def describe(wl, prec=None):
     return (f"{wl.name}: {len(wl.doc_lens)} x {wl.max_seqlen} tokens (T={wl.total_tokens}), {wl.n_heads} heads, "
             f"D={wl.head_dim} ({wl.rope_dim} RoPE + {wl.head_dim - wl.rope_dim} NoPE), top-k {wl.index_topk}, "
-            f"{wl.prec.upper()} scoring" + (", key LayerNorm + RoPE in FP32" if wl.layernorm else ""))
+            f"{(prec or wl.prec).upper()} scoring" + (", key LayerNorm + RoPE in FP32" if wl.layernorm else ""))
 
 
 def load_peaks():
@@ -200,7 +200,7 @@ def run_table(args):
     peaks, peak_kind = load_peaks()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=devn)
     cases = [("tiny", "bf16"), ("c2", "bf16"), ("c3", "mxfp8"), ("c3", "bf16"), ("thd", "mxfp8"),
-             ("kpool", "bf16"), ("target", "mxfp8"), ("target", "bf16")]
+             ("kpool", "bf16"), ("target", "mxfp8"), ("target", "bf16"), ("target", "fp8")]
     print(f"| config | precision | score+top-k ms | queries/s | TFLOP/s | % of {peak_kind} peak | "
           f"oracle queries/s ({os.cpu_count()} cores, rows) |")
     print("|---|---|---:|---:|---:|---:|---:|")
@@ -242,10 +242,10 @@ def run_table(args):
             raise RuntimeError(f"{name} {prec}: device status {dsa.read_status(ws)}")
         ms = statistics.median(ts)
         tf = wl.flops() / ms / 1e9
-        peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if prec == "mxfp8" else 1.0)
+        peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if prec in ("mxfp8", "fp8") else 1.0)
         n_rows = min(T, args.ref_rows // 8 if T > 4096 else 64)
         orate, _ = oracle_rate(wl, x, prec, n_rows)
-        print(f"| {describe(wl)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
+        print(f"| {describe(wl, prec)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
               f"{100 * tf / peak:.1f} | {orate:,.1f} ({n_rows}) |", flush=True)
 
 

@@ -71,7 +71,10 @@ typedef enum {
 
 typedef enum { DSA_DTYPE_F32 = 0, DSA_DTYPE_BF16 = 1 } dsa_dtype_t;
 
-typedef enum { DSA_PREC_BF16 = 0, DSA_PREC_MXFP8 = 1 } dsa_precision_t;
+/* Scoring precision.  DSA_PREC_FP8: E4M3 with one UE8M0 scale per vector
+ * (the SM90 path's per-vector FP8 scoring, [P1] "What does this PR do?"):
+ * q_scale [rows of q] and k_scale [rows of k] hold one byte per row. */
+typedef enum { DSA_PREC_BF16 = 0, DSA_PREC_MXFP8 = 1, DSA_PREC_FP8 = 2 } dsa_precision_t;
 
 /* UE8M0 block-exponent rule of the MXFP8 quantiser.
  * DSA_MX_SCALE_NOSAT (default): the smallest e with amax <= 448*2^e, so no
@@ -124,10 +127,12 @@ int dsa_idx_output_width(int index_topk, int kpool_size, int flags);
  *             every document
  *   rope_interleaved  0: rotate-half pairs (i, i+rope_dim/2); 1: pairs (2i, 2i+1)
  *   out_prec BF16: q_out/k_out are bf16; MXFP8: e4m3 bytes + UE8M0 scales
+ *           per 32 elements; FP8: e4m3 bytes + one UE8M0 scale per row
  *   q_out   device [total_tokens*n_heads, head_dim] (bf16 or u8)
- *   q_scale_out device u8 [total_tokens*n_heads, head_dim/32] (MXFP8 only, else NULL)
+ *   q_scale_out device u8 [total_tokens*n_heads, head_dim/32] (MXFP8) or
+ *           [total_tokens*n_heads] (FP8), else NULL
  *   k_out, k_scale_out  same for the keys ([total_tokens, ...])
- * Supported: head_dim in {64,128} (MXFP8: 128), n_heads in {1..64}. */
+ * Supported: head_dim in {64,128} (MXFP8 and FP8: 128), n_heads in {1..64}. */
 dsa_status_t dsa_idx_preprocess(
     const void* q, const void* k, dsa_dtype_t in_dtype,
     const float* ln_gamma, const float* ln_beta, float ln_eps,
@@ -144,6 +149,19 @@ dsa_status_t dsa_idx_preprocess(
  *   x_e4m3   device u8 [rows, cols]
  *   x_ue8m0  device u8 [rows, cols/32]
  * cols must be a multiple of 32 (64 or 128 for the scoring kernel). */
+/* Stand-alone BF16/FP32 -> FP8 with one UE8M0 scale per row (the per-vector
+ * FP8 scoring of [P1] "What does this PR do?"); the row exponent follows the
+ * same rule as an MXFP8 block (scale_rule).
+ *   x        device [rows, 128] in_dtype, 16-byte aligned
+ *   x_e4m3   device u8 [rows, 128]
+ *   x_ue8m0  device u8 [rows]
+ * cols must be 128 (DSA_ERR_UNSUPPORTED otherwise). */
+dsa_status_t dsa_idx_quantize_fp8_rows(const void* x, dsa_dtype_t in_dtype,
+                                       int64_t rows, int cols,
+                                       dsa_mx_scale_rule_t scale_rule,
+                                       uint8_t* x_e4m3, uint8_t* x_ue8m0,
+                                       dsa_stream_t stream);
+
 dsa_status_t dsa_idx_quantize_mxfp8(const void* x, dsa_dtype_t in_dtype,
                                     int64_t rows, int cols,
                                     dsa_mx_scale_rule_t scale_rule,
@@ -173,15 +191,19 @@ dsa_status_t dsa_idx_kpool_compress(
  * T x S score matrix on chip.  ([P1] findings 1-3, [P2] "Key changes",
  * [P3] "Changes" for pool mode.)
  *   q        device [total_tokens*n_heads, head_dim]: bf16 (BF16) or e4m3 (MXFP8)
- *   q_scale  device u8 [total_tokens*n_heads, head_dim/32] (MXFP8), else NULL
+ *   q_scale  device u8 [total_tokens*n_heads, head_dim/32] (MXFP8) or
+ *            [total_tokens*n_heads] (FP8), else NULL
  *   k        device [total_tokens, head_dim]; in pool mode the pooled keys
  *            [total_tokens/kpool_size, head_dim] from dsa_idx_kpool_compress
- *   k_scale  device u8 [rows of k, head_dim/32] (MXFP8), else NULL
+ *   k_scale  device u8 [rows of k, head_dim/32] (MXFP8) or [rows of k] (FP8),
+ *            else NULL
  *   w        device [total_tokens, n_heads], w_dtype (FP32 or BF16)
  *   sm_scale scalar multiplier of the score
  *   index_topk  keys selected per query; in pool mode a multiple of
  *               kpool_size, and index_topk / kpool_size pools are kept
- *   prec     BF16 (kind::f16) or MXFP8 (block-scaled kind::mxf8f6f4)
+ *   prec     BF16 (kind::f16), MXFP8 (block-scaled kind::mxf8f6f4) or FP8
+ *            (kind::f8f6f4; the per-row scales are folded exactly into the
+ *            head weights and the key's score, as powers of two)
  *   flags    DSA_FLAG_* bits
  *   kpool_size  1 = plain keys; >1 = pool mode (cu_pools required): KPool
  *               pools of that size (2, 4 or 8), or with
@@ -205,7 +227,7 @@ dsa_status_t dsa_idx_kpool_compress(
  *   ws, ws_bytes  device workspace of dsa_idx_workspace_size() bytes
  * Ties are broken towards the lower index; -0 and +0 compare equal.
  * Supported: head_dim 128 (BF16 also 64), n_heads in {4,8,16,32,64},
- * 1 <= index_topk <= 2048 (MXFP8 with 4 heads: <= 1664, the candidate
+ * 1 <= index_topk <= 2048 (MXFP8 or FP8 with 4 heads: <= 1664, the candidate
  * buffers of its 12 queries per block must fit in shared memory),
  * max_seqlen <= 65536.  Other shapes return DSA_ERR_UNSUPPORTED. */
 dsa_status_t dsa_idx_score_topk(

@@ -16,10 +16,10 @@ import torch
 from . import _abi
 from ._abi import (DSA_FLAG_COMPRESSED_KEYS, DSA_FLAG_DETERMINISTIC, DSA_FLAG_KPOOL_TAIL,  # noqa: F401
                    DSA_FLAG_SORT_BY_SCORE,
-                   DSA_PREC_BF16, DSA_PREC_MXFP8)
+                   DSA_PREC_BF16, DSA_PREC_FP8, DSA_PREC_MXFP8)
 
 __all__ = [
-    "DsaError", "preprocess", "quantize_mxfp8", "kpool_compress", "score_topk", "score_topk_kv", "workspace",
+    "DsaError", "preprocess", "quantize_mxfp8", "quantize_fp8_rows", "kpool_compress", "score_topk", "score_topk_kv", "workspace",
     "read_status", "debug_mma_tile", "output_width",
 ]
 
@@ -55,7 +55,7 @@ def _stream() -> int:
 def _prec(p) -> int:
     if isinstance(p, int):
         return p
-    return {"bf16": DSA_PREC_BF16, "mxfp8": DSA_PREC_MXFP8}[p]
+    return {"bf16": DSA_PREC_BF16, "mxfp8": DSA_PREC_MXFP8, "fp8": DSA_PREC_FP8}[p]
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -104,8 +104,9 @@ def preprocess(q: torch.Tensor, k: torch.Tensor, cu_seqlens: torch.Tensor, max_s
         else:
             q_op = torch.empty((T * H, D), dtype=torch.uint8, device=q.device)
             k_op = torch.empty((T, D), dtype=torch.uint8, device=q.device)
-            q_sc = torch.empty((T * H, D // 32), dtype=torch.uint8, device=q.device)
-            k_sc = torch.empty((T, D // 32), dtype=torch.uint8, device=q.device)
+            ns = 1 if prec == DSA_PREC_FP8 else D // 32   # scales per row
+            q_sc = torch.empty((T * H, ns), dtype=torch.uint8, device=q.device)
+            k_sc = torch.empty((T, ns), dtype=torch.uint8, device=q.device)
     else:
         q_op, q_sc, k_op, k_sc = out
     lib = _abi.load()
@@ -127,6 +128,18 @@ def quantize_mxfp8(x: torch.Tensor, scale_rule="nosat") -> Tuple[torch.Tensor, t
     code = _abi.load().dsa_idx_quantize_mxfp8(_ptr(x2), _dtype(x2), rows, cols, _rule(scale_rule),
                                               _ptr(codes), _ptr(scales), _stream())
     _check(code, "dsa_idx_quantize_mxfp8")
+    return codes, scales
+
+
+def quantize_fp8_rows(x: torch.Tensor, scale_rule="nosat") -> Tuple[torch.Tensor, torch.Tensor]:
+    """BF16/FP32 [rows, 128] -> (E4M3 codes uint8 [rows, 128], UE8M0 uint8 [rows]): one scale per row."""
+    x2 = x.reshape(-1, x.shape[-1])
+    rows, cols = x2.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows,), dtype=torch.uint8, device=x.device)
+    code = _abi.load().dsa_idx_quantize_fp8_rows(_ptr(x2), _dtype(x2), rows, cols, _rule(scale_rule),
+                                                 _ptr(codes), _ptr(scales), _stream())
+    _check(code, "dsa_idx_quantize_fp8_rows")
     return codes, scales
 
 

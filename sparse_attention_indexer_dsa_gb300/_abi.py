@@ -23,6 +23,7 @@ DSA_DTYPE_BF16 = 1
 # dsa_precision_t
 DSA_PREC_BF16 = 0
 DSA_PREC_MXFP8 = 1
+DSA_PREC_FP8 = 2
 # dsa_mx_scale_rule_t
 DSA_MX_SCALE_NOSAT = 0
 DSA_MX_SCALE_FLOOR = 1
@@ -45,6 +46,7 @@ SIGNATURES = {
                                     _c_int, _c_int, _c_int, _c_f, _c_int, _c_int, _c_int, _c_int,
                                     _vp, _vp, _vp, _vp, _vp]),
     "dsa_idx_quantize_mxfp8": (_c_int, [_vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp, _vp]),
+    "dsa_idx_quantize_fp8_rows": (_c_int, [_vp, _c_int, _c_i64, _c_int, _c_int, _vp, _vp, _vp]),
     "dsa_idx_kpool_compress": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                         _vp, _vp, _vp]),
     "dsa_idx_score_topk": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_f, _vp, _c_int, _c_int,

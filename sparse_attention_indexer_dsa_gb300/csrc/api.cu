@@ -202,6 +202,9 @@ dsa_status_t dsa_idx_preprocess(const void* q, const void* k, dsa_dtype_t in_dty
     if (head_dim != 128) return fail(DSA_ERR_UNSUPPORTED, "MXFP8 output needs head_dim 128");
     if (!q_scale_out || !k_scale_out || !aligned16(q_scale_out) || !aligned16(k_scale_out))
       return fail(DSA_ERR_INVALID_ARG, "MXFP8 output needs 16-byte aligned scale buffers");
+  } else if (out_prec == DSA_PREC_FP8) {
+    if (head_dim != 128) return fail(DSA_ERR_UNSUPPORTED, "FP8 output needs head_dim 128");
+    if (!q_scale_out || !k_scale_out) return fail(DSA_ERR_INVALID_ARG, "FP8 output needs scale buffers");
   } else if (out_prec != DSA_PREC_BF16) {
     return fail(DSA_ERR_INVALID_ARG, "out_prec");
   }
@@ -223,10 +226,28 @@ dsa_status_t dsa_idx_preprocess(const void* q, const void* k, dsa_dtype_t in_dty
   p.rope_dim = rope_dim;
   p.interleaved = rope_interleaved ? 1 : 0;
   p.rope_fp32 = rope_fp32 ? 1 : 0;
-  p.out_mx = out_prec == DSA_PREC_MXFP8;
+  p.out_mode = out_prec == DSA_PREC_MXFP8 ? 1 : (out_prec == DSA_PREC_FP8 ? 2 : 0);
   p.scale_rule = (int)scale_rule;
   cudaError_t e = launch_preprocess(p, head_dim, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_idx_quantize_fp8_rows(const void* x, dsa_dtype_t in_dtype, int64_t rows, int cols,
+                                       dsa_mx_scale_rule_t scale_rule, uint8_t* x_e4m3, uint8_t* x_ue8m0,
+                                       dsa_stream_t stream) {
+  if (!x || !x_e4m3 || !x_ue8m0) return fail(DSA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(x_e4m3)) return fail(DSA_ERR_INVALID_ARG, "16-byte alignment");
+  if (rows < 0 || cols != 128) return fail(DSA_ERR_UNSUPPORTED, "cols must be 128");
+  if (in_dtype != DSA_DTYPE_F32 && in_dtype != DSA_DTYPE_BF16) return fail(DSA_ERR_INVALID_ARG, "in_dtype");
+  if (scale_rule != DSA_MX_SCALE_NOSAT && scale_rule != DSA_MX_SCALE_FLOOR)
+    return fail(DSA_ERR_INVALID_ARG, "scale_rule");
+  DevInfo di;
+  dsa_status_t s = device_info(&di);
+  if (s != DSA_OK) return s;
+  cudaError_t e = launch_quantize_fp8_rows(x, in_dtype == DSA_DTYPE_BF16, rows, (int)scale_rule, x_e4m3, x_ue8m0,
+                                           di.sm_count, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return DSA_OK;
 }
 
@@ -289,11 +310,15 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   if (max_seqlen > 65536 || max_seqlen_k > 65536) return fail(DSA_ERR_UNSUPPORTED, "max_seqlen above 65536");
   if (cu_k && kpool_size > 1) return fail(DSA_ERR_UNSUPPORTED, "pool mode with separate key lengths");
   if (!heads_ok(n_heads)) return fail(DSA_ERR_UNSUPPORTED, "n_heads must be 4, 8, 16, 32 or 64");
-  if (prec != DSA_PREC_BF16 && prec != DSA_PREC_MXFP8) return fail(DSA_ERR_INVALID_ARG, "prec");
+  if (prec != DSA_PREC_BF16 && prec != DSA_PREC_MXFP8 && prec != DSA_PREC_FP8)
+    return fail(DSA_ERR_INVALID_ARG, "prec");
   if (prec == DSA_PREC_MXFP8) {
     if (head_dim != 128) return fail(DSA_ERR_UNSUPPORTED, "MXFP8 scoring needs head_dim 128");
     if (!q_scale || !k_scale || !aligned16(q_scale) || !aligned16(k_scale))
       return fail(DSA_ERR_INVALID_ARG, "MXFP8 needs 16-byte aligned q_scale and k_scale");
+  } else if (prec == DSA_PREC_FP8) {
+    if (head_dim != 128) return fail(DSA_ERR_UNSUPPORTED, "FP8 scoring needs head_dim 128");
+    if (!q_scale || !k_scale) return fail(DSA_ERR_INVALID_ARG, "FP8 needs q_scale and k_scale");
   } else if (head_dim != 64 && head_dim != 128) {
     return fail(DSA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   }
@@ -324,18 +349,19 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
     return fail(DSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, ws_total(ws_tokens, num_seqs, mxw));
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(DSA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   ScoreParams p{};
-  const int pl_prec = prec == DSA_PREC_MXFP8 ? PREC_MXFP8 : PREC_BF16;
+  const int pl_prec = prec == DSA_PREC_MXFP8 ? PREC_MXFP8 : (prec == DSA_PREC_FP8 ? PREC_FP8 : PREC_BF16);
   if (!make_score_plan(pl_prec, head_dim, n_heads, keep, &p.plan))
     return fail(DSA_ERR_UNSUPPORTED, "no kernel configuration fits (n_heads %d, keep %d)", n_heads, keep);
   DevInfo di;
   dsa_status_t s = device_info(&di);
   if (s != DSA_OK) return s;
-  const bool fp8 = pl_prec == PREC_MXFP8;
+  const bool fp8 = pl_prec != PREC_BF16;          // one-byte operands
+  const bool mx = pl_prec == PREC_MXFP8;          // block scales through TMEM
   const int64_t krows = kpool_size > 1 ? total_tokens / kpool_size : total_k;
   if ((s = make_operand_map(&p.tm_q, q, (int64_t)total_tokens * n_heads, head_dim, fp8, p.plan.ncols)) != DSA_OK)
     return s;
   if ((s = make_operand_map(&p.tm_k, k, krows, head_dim, fp8)) != DSA_OK) return s;
-  if (fp8) {
+  if (mx) {
     if ((s = make_scale_map(&p.tm_qs, q_scale, (int64_t)total_tokens * n_heads)) != DSA_OK) return s;
     if ((s = make_scale_map(&p.tm_ks, k_scale, krows)) != DSA_OK) return s;
   }
@@ -357,7 +383,10 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   p.items = items;
   p.hdr = hdr;
   p.tile_base = tile_base;
-  p.ksf_tiles = fp8 ? ksf_tiles : nullptr;
+  p.ksf_tiles = mx ? ksf_tiles : nullptr;
+  p.q_scale_vec = pl_prec == PREC_FP8 ? q_scale : nullptr;
+  p.k_scale_vec = pl_prec == PREC_FP8 ? k_scale : nullptr;
+  p.k_rows = krows;
   p.timeout_ns = g_timeout_ns;
   p.sm_scale = sm_scale;
   p.w_bf16 = w_dtype == DSA_DTYPE_BF16;
@@ -372,7 +401,7 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
                                         tile_base, hdr, max_items, st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   if (total_tokens == 0) return DSA_OK;
-  if (fp8) {
+  if (mx) {
     e = launch_tiled_kscales(k_scale, krows, p.cu_keys, tile_base, num_seqs,
                              ws_ksf_tiles(ws_tokens, num_seqs), ksf_tiles, di.sm_count, st);
     if (e != cudaSuccess) return cuda_fail(e, "key-scale layout launch");

@@ -21,7 +21,8 @@ struct PreParams {
   uint8_t* k_scale;
   double inv_freq[64];
   float eps;
-  int in_bf16, num_seqs, total_tokens, H, rope_dim, interleaved, rope_fp32, out_mx, scale_rule;
+  int in_bf16, num_seqs, total_tokens, H, rope_dim, interleaved, rope_fp32, scale_rule;
+  int out_mode;   // 0: BF16, 1: MXFP8 (scale per 32 elements), 2: FP8 (scale per row)
 };
 
 struct DebugParams {
@@ -34,6 +35,8 @@ struct DebugParams {
 };
 
 cudaError_t launch_preprocess(const PreParams& p, int D, cudaStream_t stream);
+cudaError_t launch_quantize_fp8_rows(const void* x, int in_bf16, int64_t rows, int rule, uint8_t* out,
+                                     uint8_t* scales, int sm_count, cudaStream_t stream);
 cudaError_t launch_quantize_mxfp8(const void* x, int in_bf16, int64_t nblocks, int rule,
                                   uint8_t* out, uint8_t* scales, int sm_count, cudaStream_t stream);
 cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const float* bias,

@@ -1,4 +1,5 @@
-// Query/key preprocessing and MXFP8 quantisation for sm_103a (HBM-bound).
+// Query/key preprocessing and MXFP8 / per-vector FP8 quantisation for sm_103a
+// (HBM-bound).
 //
 // * preprocess_kernel: key LayerNorm -> RoPE -> BF16 or MXFP8, one block per
 //   token (its H query rows + its key row), one warp per row, 128-bit loads,
@@ -60,12 +61,15 @@ __device__ __forceinline__ float exp2_neg(int e) {
   return be >= 1 ? __uint_as_float((uint32_t)be << 23) : __uint_as_float(0x00400000u);
 }
 
-// Quantise one 32-element block spread over 8 consecutive lanes (4 values per
-// lane).  Returns the lane's 4 payload bytes; *scale_byte is the block's UE8M0.
-__device__ __forceinline__ uint32_t mx_quant_lane4(const float v[4], int rule, int* scale_byte) {
+// Quantise one block of 4*GL elements spread over GL consecutive lanes (4
+// values per lane): GL = 8 is an MXFP8 block of 32, GL = 32 a whole 128-element
+// row of per-vector FP8.  Returns the lane's 4 payload bytes; *scale_byte is
+// the block's UE8M0.
+template <int GL>
+__device__ __forceinline__ uint32_t quant_lane4(const float v[4], int rule, int* scale_byte) {
   float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int o = 1; o < GL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int e = mx_exponent(amax, rule);
   const float mul = exp2_neg(e);
   const __nv_fp8x2_storage_t lo =
@@ -210,10 +214,17 @@ __global__ void __launch_bounds__(kPreThreads) preprocess_kernel(const __grid_co
     }
     const size_t orow = is_key ? (size_t)t : (size_t)t * H + r;
     void* out = is_key ? p.k_out : p.q_out;
-    if (p.out_mx) {
+    if (p.out_mode == 2) {   // FP8, one scale per row (D = 128: 4 values per lane)
       if constexpr (VEC == 4) {
         int sb;
-        const uint32_t pay = mx_quant_lane4(v, p.scale_rule, &sb);
+        const uint32_t pay = quant_lane4<32>(v, p.scale_rule, &sb);
+        reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
+        if (lane == 0) (is_key ? p.k_scale : p.q_scale)[orow] = (uint8_t)sb;
+      }
+    } else if (p.out_mode == 1) {
+      if constexpr (VEC == 4) {
+        int sb;
+        const uint32_t pay = quant_lane4<8>(v, p.scale_rule, &sb);
         reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
         const int s1 = __shfl_sync(0xffffffffu, sb, 8), s2 = __shfl_sync(0xffffffffu, sb, 16),
                   s3 = __shfl_sync(0xffffffffu, sb, 24);
@@ -267,12 +278,39 @@ __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const void* __restr
       }
     }
     int sb;
-    const uint32_t pay = mx_quant_lane4(v, rule, &sb);
+    const uint32_t pay = quant_lane4<8>(v, rule, &sb);
     if (valid) {
       reinterpret_cast<uint32_t*>(out)[e0 >> 2] = pay;
       if ((lane & 7) == 0) scales[blk] = (uint8_t)sb;
     }
   }
+}
+
+// Per-vector FP8: one warp per 128-element row, 4 elements per lane.
+__global__ void __launch_bounds__(256) quantize_fp8_rows_kernel(const void* __restrict__ x, int in_bf16,
+                                                               int64_t rows, int rule,
+                                                               uint8_t* __restrict__ out,
+                                                               uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    float v[4];
+    load_row<4>(x, in_bf16, (size_t)r, 128, lane, v);
+    int sb;
+    const uint32_t pay = quant_lane4<32>(v, rule, &sb);
+    reinterpret_cast<uint32_t*>(out)[r * 32 + lane] = pay;
+    if (lane == 0) scales[r] = (uint8_t)sb;
+  }
+}
+
+cudaError_t launch_quantize_fp8_rows(const void* x, int in_bf16, int64_t rows, int rule, uint8_t* out,
+                                     uint8_t* scales, int sm_count, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)sm_count * 16;
+  if (blocks > cap) blocks = cap;
+  quantize_fp8_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, in_bf16, rows, rule, out, scales);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_preprocess(const PreParams& p, int D, cudaStream_t stream) {

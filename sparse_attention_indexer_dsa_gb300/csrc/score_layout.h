@@ -7,7 +7,7 @@
 
 namespace dsa {
 
-enum { PREC_BF16 = 0, PREC_MXFP8 = 1 };
+enum { PREC_BF16 = 0, PREC_MXFP8 = 1, PREC_FP8 = 2 };   // FP8: one scale per row
 
 constexpr int kEpiWarp0 = 2;         // warp 0: TMA producer, warp 1: MMA + TMEM owner, then epilogue
 constexpr int kMaxEpiWGs = 4;
@@ -34,9 +34,9 @@ __host__ __device__ constexpr int epi_wgs(int prec) { return prec == PREC_BF16 ?
 __host__ __device__ constexpr int score_threads(int prec) { return 64 + 128 * epi_wgs(prec); }
 // Batches between two abort / shrink votes.  Voting every other batch saves a
 // block-wide barrier per batch but needs room for two batches after a shrink:
-// only the MXFP8 64-head plan has candidate buffers large enough for that.
+// only the 8-bit 64-head plans have candidate buffers large enough for that.
 __host__ __device__ constexpr int vote_every(int prec, int n_heads) {
-  return prec == PREC_MXFP8 && n_heads == 64 ? 2 : 1;
+  return prec != PREC_BF16 && n_heads == 64 ? 2 : 1;
 }
 __host__ __device__ constexpr int qpw_max(int prec, int n_heads) {
   return max_ncols(prec) / (epi_wgs(prec) * n_heads) < kMaxQpw ? max_ncols(prec) / (epi_wgs(prec) * n_heads)
@@ -78,6 +78,9 @@ struct ScoreParams {
   int* hdr;                 // [0] status, [1] item count
   const int* tile_base;     // first key tile of each document in ksf_tiles
   const uint32_t* ksf_tiles;   // MXFP8: key scales laid out per key tile for tcgen05.cp (512 B each)
+  const uint8_t* q_scale_vec;  // FP8: one UE8M0 byte per q row [T*H]
+  const uint8_t* k_scale_vec;  // FP8: one UE8M0 byte per key row
+  int64_t k_rows;              // rows of the key operand
   unsigned long long timeout_ns;
   float sm_scale;
   int w_bf16;

@@ -611,6 +611,8 @@ template <int PREC, int H>
 __global__ void __launch_bounds__(score_threads(PREC), 1)
     score_topk_kernel(const __grid_constant__ ScoreParams p) {
   constexpr bool MX = PREC == PREC_MXFP8;
+  constexpr bool F8 = PREC == PREC_FP8;                // one UE8M0 scale per row, folded in the epilogue
+  constexpr bool B1 = MX || F8;                        // one-byte operands
   constexpr int EW = epi_wgs(PREC);                   // epilogue warpgroups
   constexpr int QPW_MAX = qpw_max(PREC, H);           // queries per epilogue warpgroup
   constexpr int NCOLW = QPW_MAX * H;                  // accumulator columns a thread reads per tile
@@ -683,7 +685,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
       bool ok = true;
       const uint32_t q_bytes = pl.chunks * pl.qchunk + (MX ? pl.sfb_atoms * kSfRawWords * 4 : 0);
       const uint32_t k_bytes = kStageBytes + (MX ? kSfTxBytes : 0);
-      const int chunk_elems = kChunkBytes / (MX ? 1 : 2);
+      const int chunk_elems = kChunkBytes / (B1 ? 1 : 2);
       for (int r = 0; ok && r * G < nitems; ++r) {
         const int i = item_index(r, nitems);
         if (i < 0) continue;
@@ -751,7 +753,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
     uint32_t tcount = 0, st = 0, ph = 0;
     int it = 0;
     bool ok = true;
-    const uint32_t idesc = MX ? 0u : idesc_bf16(128, pl.ncols);
+    const uint32_t idesc = MX ? 0u : (F8 ? idesc_f8(128, pl.ncols) : idesc_bf16(128, pl.ncols));
     uint32_t idesc_k[4];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) idesc_k[kk] = idesc_mxf8(128, pl.ncols, kk);
@@ -818,6 +820,8 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
               if (MX)
                 mma_mxf8(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc_k[kk], sfa, tmem + kSfbCol, acc);
+              else if (F8)
+                mma_f8(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
               else
                 mma_bf16(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
             }
@@ -886,6 +890,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
           const size_t off = (size_t)(a + t) * H + (e % H);
           wv = p.w_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])
                         : reinterpret_cast<const float*>(p.w)[off];
+          if (F8) wv = ldexpf(wv, (int)p.q_scale_vec[off] - 127);   // the q row's scale folded into w
         }
         w_s[e] = wv;
       }
@@ -907,6 +912,12 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         for (int i = 0; i < 8; ++i) wp[i] = *reinterpret_cast<const float2*>(w_s + 8 * i + 2 * (lane & 3));
       }
       PT_ADD(5);
+      // FP8: UE8M0 byte of this thread's key row (local key index s), 127 past the end
+      auto key_scale_byte = [&](int s) -> int {
+        const int64_t krow = (int64_t)m.krow0 + s;
+        return krow < p.k_rows ? (int)__ldg(p.k_scale_vec + krow) : 127;
+      };
+      int kexp = F8 && m.ntiles > 0 ? key_scale_byte(row) : 127;
       for (int tb = 0; tb < m.ntiles; tb += kBatch) {
         // ---- score kBatch tiles; keep keys and ballots in registers ----
         uint32_t bkey[kBatch][QPW_MAX];
@@ -927,6 +938,13 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             TRACE(2 + v, tcount, tid == 0);   // warpgroup v woke on the tile's accumulator
             tc_fence_after();
             const int s_idx = t * kTileKeys + row;      // local key (or pool) index
+            // FP8: the key row's scale multiplies its score (sm_scale folded in);
+            // the next tile's scale byte is fetched now, a tile ahead of its use
+            float kfac = p.sm_scale;
+            if (F8) {
+              kfac = ldexpf(p.sm_scale, kexp - 127);
+              if (t + 1 < m.ntiles) kexp = key_scale_byte(s_idx + kTileKeys);
+            }
             if constexpr (FRAG) {
               // Fragment layout (.16x256b): thread t holds 16 heads (2(t%4) + 8i, +1) of
               // the four key rows g, g+8, g+16, g+24 (g = t/4) of its warp's 32 rows, so
@@ -984,7 +1002,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               const float k1 = (b1 ? s3 : s1) + __shfl_xor_sync(0xffffffffu, b1 ? s1 : s3, 2);
               const float own = (b0 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b0 ? k0 : k1, 1);
               // row r's total sits in lane 4 (r % 8) + r / 8
-              const float sv = __shfl_sync(0xffffffffu, own, 4 * (lane & 7u) + (lane >> 3)) * p.sm_scale;
+              const float sv = __shfl_sync(0xffffffffu, own, 4 * (lane & 7u) + (lane >> 3)) * kfac;
               const bool vis = s_idx <= vis_lim[0];
               bkey[b][0] = orderable_key(sv);
               bbal[b][0] = __ballot_sync(0xffffffffu, vis && bkey[b][0] > tau[0]);
@@ -1036,7 +1054,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
                   float sv = 0.f;
 #pragma unroll
                   for (int c = 0; c < NCH; ++c) sv += part[qi][c].x + part[qi][c].y;
-                  sv *= p.sm_scale;
+                  sv *= kfac;
                   const bool vis = s_idx <= vis_lim[qi];
                   bkey[b][qi] = orderable_key(sv);
                   bbal[b][qi] = __ballot_sync(0xffffffffu, vis && bkey[b][qi] > tau[qi]);
@@ -1316,6 +1334,16 @@ static cudaError_t launch_score_t(const ScoreParams& p, int grid, cudaStream_t s
 
 cudaError_t launch_score_topk(const ScoreParams& p, int grid, cudaStream_t stream) {
   const int H = p.plan.n_heads;
+  if (p.plan.prec == PREC_FP8) {
+    switch (p.plan.n_heads) {
+      case 4: return launch_score_t<PREC_FP8, 4>(p, grid, stream);
+      case 8: return launch_score_t<PREC_FP8, 8>(p, grid, stream);
+      case 16: return launch_score_t<PREC_FP8, 16>(p, grid, stream);
+      case 32: return launch_score_t<PREC_FP8, 32>(p, grid, stream);
+      case 64: return launch_score_t<PREC_FP8, 64>(p, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (p.plan.prec == PREC_BF16) {
     switch (H) {
       case 4: return launch_score_t<PREC_BF16, 4>(p, grid, stream);

@@ -174,3 +174,59 @@ def test_preprocess_mxfp8_out(case):
     assert np.all(err <= np.ldexp(1.0, host(q_sc).astype(int).repeat(32, axis=1) - 127 + 8 - 3) + 1e-30)
     errk = np.abs(gk - rk)
     assert np.all(errk <= np.ldexp(1.0, host(k_sc).astype(int).repeat(32, axis=1) - 127 + 8 - 3) + 1e-30)
+
+
+@pytest.mark.parametrize("rule", ["nosat", "floor"])
+@pytest.mark.parametrize("src", ["f32", "bf16"])
+def test_quantize_fp8_rows_bit_exact(rule, src):
+    """Per-vector FP8 (one UE8M0 scale per 128-element row) against the
+    oracle's quantize_fp8_rows on identical input, bit for bit."""
+    rng = np.random.default_rng(15)
+    x = _edge_rows(rng)
+    x = np.concatenate([x, (rng.standard_normal((1000, 128)) * np.exp2(rng.integers(-30, 30, (1000, 1)))).astype(np.float32)])
+    if src == "bf16":
+        bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+        xin = bf16_dev(bits)
+        xv = O.bf16_bits_to_float(bits)
+    else:
+        xin = dev(x)
+        xv = x.astype(np.float64)
+    codes, scales = dsa.quantize_fp8_rows(xin, rule)
+    rc, rs, _ = O.quantize_fp8_rows(xv, rule)
+    np.testing.assert_array_equal(host(scales), rs)
+    np.testing.assert_array_equal(host(codes), rc)
+
+
+@pytest.mark.parametrize("case", CASES[:4], ids=[str(i) for i in range(4)])
+def test_preprocess_fp8_out(case):
+    """Fused preprocess with per-vector FP8 output: the GPU's FP32 carrier
+    and the oracle's float64 one differ by FP32 rounding only, so scale bytes
+    agree almost everywhere and every value is within one E4M3 step."""
+    rng = np.random.default_rng(16)
+    lens, H, D = case["lens"], case["H"], case["D"]
+    if D != 128:
+        pytest.skip("FP8 output needs head_dim 128")
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = rng.standard_normal((T, H, D)).astype(np.float32)
+    k = rng.standard_normal((T, D)).astype(np.float32)
+    g = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(D)).astype(np.float32)
+    gd, bd = (dev(g), dev(b)) if case["ln"] else (None, None)
+    q_op, q_sc, k_op, k_sc = dsa.preprocess(dev(q), dev(k), dev(cu), max(lens), gd, bd, 1e-6, case["rope"],
+                                            10000.0, case["inter"], case["fp32"], "fp8")
+    qf, kf = O.preprocess(q, k, cu, g if case["ln"] else None, b if case["ln"] else None, 1e-6,
+                          case["rope"], 10000.0, case["inter"], case["fp32"])
+    _, rqs, rq = O.quantize_fp8_rows(qf.reshape(T * H, D))
+    _, rks, rk = O.quantize_fp8_rows(kf)
+    gqs, gks = host(q_sc).reshape(-1), host(k_sc).reshape(-1)
+    gq = O.e4m3_decode(host(q_op)) * np.ldexp(1.0, gqs.astype(int) - 127)[:, None]
+    gk = O.e4m3_decode(host(k_op)) * np.ldexp(1.0, gks.astype(int) - 127)[:, None]
+    assert np.mean(gqs == rqs) > 0.999 and np.mean(gks == rks) > 0.99
+    same = gqs == rqs
+    assert np.mean(gq[same] == rq[same]) > 0.999
+    # one E4M3 step in the top binade of the coarser of the two scales
+    step = np.ldexp(1.0, np.maximum(gqs, rqs).astype(int) - 127 + 8 - 3)[:, None]
+    assert np.all(np.abs(gq - rq) <= step + 1e-30)
+    stepk = np.ldexp(1.0, np.maximum(gks, rks).astype(int) - 127 + 8 - 3)[:, None]
+    assert np.all(np.abs(gk - rk) <= stepk + 1e-30)

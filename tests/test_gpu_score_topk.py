@@ -403,3 +403,74 @@ def test_compressed_keys_too_few_rows_sets_status():
     dsa.score_topk(qb, None, kb, None, w, cu, 40, H, k, "bf16", kpool_size=ratio, cu_pools=cc, compressed=True,
                    ws=ws)
     assert dsa.read_status(ws) == _abi.DSA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- FP8 with per-vector scales
+
+FP8_CASES = [
+    ([600, 130], 64, 256),
+    ([1, 2, 3, 250, 513], 32, 64),
+    ([2500], 64, 2048),
+    ([389], 16, 33),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[str(i) for i in range(len(FP8_CASES))])
+def test_fp8_rows_random_operands(case):
+    """FP8 scoring with one UE8M0 scale per q row and per key (kind::f8f6f4,
+    scales folded into the head weights and the key's score): both sides
+    score identical dequantised operands, so FP32 accumulation is the only
+    difference."""
+    lens, H, k = case
+    D = 128
+    T = sum(lens)
+    rng = np.random.default_rng(131 + H + k)
+    q = rng.standard_normal((T * H, D)) * np.exp2(rng.integers(-4, 5, (T * H, 1)))
+    kk = rng.standard_normal((T, D)) * np.where(rng.random((T, D)) < 0.01, 20, 1)
+    qc, qs, qd = O.quantize_fp8_rows(q)
+    kc, ks, kd = O.quantize_fp8_rows(kk)
+    w = (rng.standard_normal((T, H)) * 0.125).astype(np.float32)
+    g_idx, g_sc, g_ln, cu = _run(dev(qc), dev(qs), dev(kc), dev(ks), dev(w), lens, H, k, "fp8", sm_scale=0.25)
+    ref = O.indexer_topk(qd.reshape(T, H, D), kd, w.astype(np.float64), cu, k, sm_scale=0.25, with_scale=True)
+    compare_topk(g_idx, g_sc, g_ln, ref, REL_BF16)
+
+
+def test_fp8_rows_integer_exact():
+    """Integers in [-3, 3] are exact in per-vector FP8 (row scale 2^-7), so the
+    indices and scores must be bit-exact, ties to the lower index."""
+    rng = np.random.default_rng(141)
+    lens, H, D, k = [900, 77], 64, 128, 300
+    T = sum(lens)
+    q = rng.integers(-3, 4, (T, H, D)).astype(np.float64)
+    kk = rng.integers(-3, 4, (T, D)).astype(np.float64)
+    w = rng.integers(-2, 3, (T, H)).astype(np.float32)
+    qc, qs, qd = O.quantize_fp8_rows(q.reshape(T * H, D))
+    kc, ks, kd = O.quantize_fp8_rows(kk)
+    assert np.array_equal(qd, q.reshape(T * H, D)) and np.array_equal(kd, kk)
+    g_idx, g_sc, g_ln, cu = _run(dev(qc), dev(qs), dev(kc), dev(ks), dev(w), lens, H, k, "fp8")
+    rows = np.concatenate([np.arange(0, 40), np.arange(860, 940), np.arange(T - 20, T)])
+    ref = O.indexer_topk(q, kk, w.astype(np.float64), cu, k, rows=rows)
+    np.testing.assert_array_equal(g_ln[rows], ref["len"])
+    np.testing.assert_array_equal(g_idx[rows], ref["idx"])
+    np.testing.assert_array_equal(g_sc[rows], ref["score"].astype(np.float32))
+
+
+def test_fp8_rows_end_to_end_with_preprocess():
+    """Key LayerNorm + RoPE + per-vector FP8 on both sides, then scoring."""
+    wl = W.Workload("c2-fp8", [1500, 300], 32, 128, 256, "fp8", "normal", layernorm=True, rope_dim=64,
+                    rope_fp32=True, w_std=1 / np.sqrt(32), seed=1008)
+    x = W.make_inputs(wl)
+    T, H, D = wl.total_tokens, wl.n_heads, wl.head_dim
+    cu = wl.cu_seqlens
+    ops = dsa.preprocess(dev(x["q"]), dev(x["k"]), dev(cu), wl.max_seqlen, dev(x["ln_gamma"]), dev(x["ln_beta"]),
+                         1e-6, 64, 10000.0, False, True, "fp8")
+    idx, sc, ln = dsa.score_topk(*ops, dev(x["w"]), dev(cu), wl.max_seqlen, H, wl.index_topk, "fp8")
+    torch.cuda.synchronize()
+    qf, kf = O.preprocess(x["q"], x["k"], cu, x["ln_gamma"], x["ln_beta"], 1e-6, 64, 10000.0, False, True)
+    _, _, qd = O.quantize_fp8_rows(qf.reshape(T * H, D))
+    _, _, kd = O.quantize_fp8_rows(kf)
+    rows = np.concatenate([np.arange(0, 30), np.arange(1400, 1530), np.arange(T - 30, T)])
+    ref = O.indexer_topk(qd.reshape(T, H, D), kd, x["w"].astype(np.float64), cu, wl.index_topk, rows=rows,
+                         with_scale=True)
+    # the two carriers differ by FP32 rounding, which can move an element by one E4M3 step
+    compare_topk(host(idx), host(sc), host(ln), ref, REL_MXFP8, rows=rows)
