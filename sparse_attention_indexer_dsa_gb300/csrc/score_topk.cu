@@ -873,7 +873,17 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
     int* hist = reinterpret_cast<int*>(smem + pl.hist_off) + v * 256;
     int* ms = reinterpret_cast<int*>(smem + pl.misc_off) + v * kMiscInts;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t lt = (1u << lane) - 1u;
+    // Key row whose score this thread reports: its own lane's row, except in
+    // the fragment layout, where lane t ends with row t/4 + 8 (t % 4) of its
+    // warp's rows; rmask marks the lanes whose rows precede it (ballot prefix in
+    // row order, so appends stay in index order).
+    const int orow = FRAG ? wq * 32 + (int)(lane >> 2) + 8 * (int)(lane & 3) : row;
+    uint32_t rmask = 0u;
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+      const int rl = FRAG ? (l >> 2) + 8 * (l & 3) : l;
+      if (rl < orow - wq * 32) rmask |= 1u << l;
+    }
     uint32_t tcount = 0, nbatch = 0;
     bool aborted = false;
     PT_DECL
@@ -917,7 +927,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         const int64_t krow = (int64_t)m.krow0 + s;
         return krow < p.k_rows ? (int)__ldg(p.k_scale_vec + krow) : 127;
       };
-      int kexp = F8 && m.ntiles > 0 ? key_scale_byte(row) : 127;
+      int kexp = F8 && m.ntiles > 0 ? key_scale_byte(orow) : 127;
       for (int tb = 0; tb < m.ntiles; tb += kBatch) {
         // ---- score kBatch tiles; keep keys and ballots in registers ----
         uint32_t bkey[kBatch][QPW_MAX];
@@ -937,7 +947,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             PT_ADD(0);
             TRACE(2 + v, tcount, tid == 0);   // warpgroup v woke on the tile's accumulator
             tc_fence_after();
-            const int s_idx = t * kTileKeys + row;      // local key (or pool) index
+            const int s_idx = t * kTileKeys + orow;     // local key (or pool) index of the reported row
             // FP8: the key row's scale multiplies its score (sm_scale folded in);
             // the next tile's scale byte is fetched now, a tile ahead of its use
             float kfac = p.sm_scale;
@@ -1001,8 +1011,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               const float k0 = (b1 ? s2 : s0) + __shfl_xor_sync(0xffffffffu, b1 ? s0 : s2, 2);
               const float k1 = (b1 ? s3 : s1) + __shfl_xor_sync(0xffffffffu, b1 ? s1 : s3, 2);
               const float own = (b0 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b0 ? k0 : k1, 1);
-              // row r's total sits in lane 4 (r % 8) + r / 8
-              const float sv = __shfl_sync(0xffffffffu, own, 4 * (lane & 7u) + (lane >> 3)) * kfac;
+              const float sv = own * kfac;   // row orow
               const bool vis = s_idx <= vis_lim[0];
               bkey[b][0] = orderable_key(sv);
               bbal[b][0] = __ballot_sync(0xffffffffu, vis && bkey[b][0] > tau[0]);
@@ -1088,9 +1097,9 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             for (int b = 0; b < kBatch; ++b) {
               const int before = (wq > 0 ? cc[b].x : 0) + (wq > 1 ? cc[b].y : 0) + (wq > 2 ? cc[b].z : 0);
               const bool mine = (bbal[b][qi] >> lane) & 1u;
-              const int pos = qi * C + count[qi] + before + __popc(bbal[b][qi] & lt);
+              const int pos = qi * C + count[qi] + before + __popc(bbal[b][qi] & rmask);
               st_shared_u32_if(mine, ckey_s + 4u * (uint32_t)pos, bkey[b][qi]);
-              st_shared_u16_if(mine, cidx_s + 2u * (uint32_t)pos, (uint16_t)((tb + b) * kTileKeys + row));
+              st_shared_u16_if(mine, cidx_s + 2u * (uint32_t)pos, (uint16_t)((tb + b) * kTileKeys + orow));
               count[qi] += cc[b].x + cc[b].y + cc[b].z + cc[b].w;
             }
           }
