@@ -32,11 +32,11 @@ constexpr int kSfbCol = 392;         // MXFP8: query scales, up to 2 atoms x 4 c
 __host__ __device__ constexpr int max_ncols(int prec) { return prec == PREC_BF16 ? 256 : 192; }
 __host__ __device__ constexpr int epi_wgs(int prec) { return prec == PREC_BF16 ? 4 : 3; }
 __host__ __device__ constexpr int score_threads(int prec) { return 64 + 128 * epi_wgs(prec); }
-// Batches between two abort / shrink votes.  Voting every other batch saves a
-// block-wide barrier per batch but needs room for two batches after a shrink:
+// Batches between two abort / shrink votes.  Voting every fourth batch saves
+// block-wide barriers but needs room for four batches after a shrink:
 // only the 8-bit 64-head plans have candidate buffers large enough for that.
 __host__ __device__ constexpr int vote_every(int prec, int n_heads) {
-  return prec != PREC_BF16 && n_heads == 64 ? 2 : 1;
+  return prec != PREC_BF16 && n_heads == 64 ? 4 : 1;
 }
 __host__ __device__ constexpr int qpw_max(int prec, int n_heads) {
   return max_ncols(prec) / (epi_wgs(prec) * n_heads) < kMaxQpw ? max_ncols(prec) / (epi_wgs(prec) * n_heads)
