@@ -27,8 +27,8 @@ requests):
 The score itself, I[t,s] = sm_scale * sum_j w[t,j] * ReLU(q[t,j] . k[s]), and
 "top-k keys per causally visible query" are what those pages imply (finding 1's
 ReLU assertion, finding 3's per-head weights and shared key head); the pages
-never print the formula.  Readings taken where the pages are silent are listed
-in the design doc and repeated at each function below.
+never print the formula.  Where the pages are silent, the reading taken is
+stated at the function it concerns.
 
 Every floating-point step is done in float64.  Rounding to the narrow formats
 (BF16, FP32, E4M3) is a single round-to-nearest-even from the float64 value,
