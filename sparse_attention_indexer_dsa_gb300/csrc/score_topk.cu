@@ -7,22 +7,27 @@
 //   I[t,s] = sm_scale * sum_j w[t,j] * ReLU(q[t,j] . k[s])  for visible s,
 //   then the `keep` best s per query t, ties to the lower index.
 //
-// Design (one persistent CTA per SM, 320 threads):
-//   * A work item is a block of Tq = 2*qs consecutive queries of one document.
-//     Its q rows (Tq*H rows of the [T*H, D] operand) stay in shared memory as
-//     two UMMA B operands ("sub-blocks", N = qs*H columns each).
+// Structure (one persistent CTA per SM; 448 threads for the 8-bit formats,
+// 576 for BF16):
+//   * A work item is nq consecutive queries of one document (one query per
+//     epilogue warpgroup at 64 heads).  Its nq*H q rows stay in shared memory
+//     as one UMMA B operand of N = nq*H columns.  Items are built and sorted
+//     longest-first on the device and dealt to CTAs in snake order.
 //   * Warp 0 streams the item's visible keys in tiles of 128 rows through a
-//     ring of shared-memory stages with TMA (128-byte swizzle).
-//   * Warp 1 issues tcgen05.mma (M = 128 keys, N = qs*H, K = head_dim) into a
-//     ring of 128-column TMEM accumulator slots; BF16 uses kind::f16, MXFP8 the
-//     block-scaled kind::mxf8f6f4 with UE8M0 scales copied into TMEM.
-//   * Warps 2..9 are two epilogue warpgroups, one per sub-block.  Thread r of a
-//     warpgroup owns key row r of the tile: it loads its row's qs*H fp32
-//     accumulators with tcgen05.ld, applies ReLU and the head weights, masks
-//     invisible keys, and offers each query's score to that query's candidate
-//     buffer in shared memory.  Candidates above the running threshold are
-//     appended in index order; when a buffer is full a radix select keeps
-//     exactly `keep` entries and raises the threshold.  Scores never reach HBM.
+//     ring of shared-memory stages with TMA (128-byte swizzle); for MXFP8 each
+//     stage also brings the tile's key scales, laid out for tcgen05.cp.
+//   * Warp 1 issues one tcgen05.mma chain per key tile (M = 128 keys, N = nq*H,
+//     K = head_dim) into a double-buffered TMEM accumulator: kind::f16 (BF16),
+//     block-scaled kind::mxf8f6f4 (MXFP8) or kind::f8f6f4 (FP8, one scale per
+//     row, folded into the epilogue).
+//   * Warps 2.. are the epilogue warpgroups (3, or 4 for BF16), one query
+//     each.  They read the accumulator with tcgen05.ld (16x256b fragments at 64
+//     heads, so each lane needs only 16 head weights), apply ReLU, the head
+//     weights and the causal mask, and offer each key's score to the query's
+//     candidate buffer in shared memory: keys above the running threshold are
+//     appended in index order, and a sampled or radix shrink keeps the buffer
+//     small and raises the threshold; a final exact radix select keeps exactly
+//     `keep` entries.  Scores never reach HBM.
 //   * Every wait is bounded (status word + abort flag, no trap); see
 //     dsa_device.cuh.
 #include <cuda_bf16.h>
