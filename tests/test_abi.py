@@ -78,14 +78,48 @@ def test_host_argument_checks_precede_any_cuda_call(lib):
     assert rc == _abi.DSA_ERR_UNSUPPORTED
 
 
+def test_host_checks_of_the_extended_modes(lib):
+    """Argument checks of the key-offset entry point, compressed keys and
+    per-vector FP8, all before any CUDA call."""
+    P = ctypes.c_void_p
+    F = _abi.DSA_FLAG_DETERMINISTIC
+    # documents with more keys than queries: cu_seqlens_k is required
+    rc = lib.dsa_idx_score_topk_kv(P(256), None, P(256), None, P(256), 0, 1.0, P(256), None, 1, 8, 16, 8, 16,
+                                   64, 128, 16, 0, F, P(256), None, None, P(256), 1 << 20, None)
+    assert rc == _abi.DSA_ERR_INVALID_ARG
+    # ... and a key length above the 16-bit index range
+    rc = lib.dsa_idx_score_topk_kv(P(256), None, P(256), None, P(256), 0, 1.0, P(256), P(256), 1, 8, 16, 8,
+                                   70000, 64, 128, 16, 0, F, P(256), None, None, P(256), 1 << 20, None)
+    assert rc == _abi.DSA_ERR_UNSUPPORTED
+    C = _abi.DSA_FLAG_COMPRESSED_KEYS
+    assert lib.dsa_idx_output_width(300, 4, C) == 300
+    # compressed keys: ratio range, cu_pools required, no KPool tail
+    for ratio, pools, flags, want in ((1, P(256), F | C, _abi.DSA_ERR_UNSUPPORTED),
+                                      (65, P(256), F | C, _abi.DSA_ERR_UNSUPPORTED),
+                                      (4, None, F | C, _abi.DSA_ERR_INVALID_ARG),
+                                      (4, P(256), F | C | _abi.DSA_FLAG_KPOOL_TAIL, _abi.DSA_ERR_INVALID_ARG)):
+        rc = lib.dsa_idx_score_topk(P(256), None, P(256), None, P(256), 0, 1.0, P(256), 1, 16, 16, 64, 128,
+                                    16, 0, flags, ratio, pools, P(256), None, None, P(256), 1 << 20, None)
+        assert rc == want, (ratio, flags, rc)
+    # per-vector FP8: head_dim 128 and both scale arrays
+    rc = lib.dsa_idx_score_topk(P(256), None, P(256), P(256), P(256), 0, 1.0, P(256), 1, 16, 16, 64, 128,
+                                16, _abi.DSA_PREC_FP8, F, 1, None, P(256), None, None, P(256), 1 << 20, None)
+    assert rc == _abi.DSA_ERR_INVALID_ARG
+    rc = lib.dsa_idx_score_topk(P(256), P(256), P(256), P(256), P(256), 0, 1.0, P(256), 1, 16, 16, 64, 64,
+                                16, _abi.DSA_PREC_FP8, F, 1, None, P(256), None, None, P(256), 1 << 20, None)
+    assert rc == _abi.DSA_ERR_UNSUPPORTED
+    rc = lib.dsa_idx_quantize_fp8_rows(P(256), 0, 4, 64, 0, P(256), P(256), None)
+    assert rc == _abi.DSA_ERR_UNSUPPORTED
+
+
 def test_score_plan_fits_every_supported_shape(lib):
     """Every supported (precision, head count, top-k) has a kernel plan; the
     planner lives in C, so probe it through the host path: a valid call with
     a zero-token batch stops at device discovery, not at planning."""
     P = ctypes.c_void_p
-    for prec, D in ((0, 128), (0, 64), (1, 128)):
+    for prec, D in ((0, 128), (0, 64), (1, 128), (2, 128)):
         for H in (4, 8, 16, 32, 64):
-            for k in ((1, 32, 256, 1024) if (prec == 1 and H == 4) else (1, 32, 256, 2048)):
+            for k in ((1, 32, 256, 1024) if (prec != 0 and H == 4) else (1, 32, 256, 2048)):
                 rc = lib.dsa_idx_score_topk(P(256), P(256), P(256), P(256), P(256), 0, 1.0, P(256), 1, 0, 0,
                                             H, D, k, prec, 1, 1, None, P(256), None, None, P(256), 1 << 20, None)
                 assert rc in (_abi.DSA_OK, _abi.DSA_ERR_CUDA, _abi.DSA_ERR_UNSUPPORTED), (prec, D, H, k, rc)
