@@ -986,16 +986,16 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
                 TRACE(6 + v, tcount, tid == 0);   // warpgroup v released the slot
               };
               uint32_t fa[32];
-              if constexpr (GRP == 64) {   // both 16-lane halves in flight at once
+              if constexpr (GRP == 64) {   // the second half loads while the first is summed
                 uint32_t fb[32];
                 tmem_ld_16x256b_x8(tcol, fa);
-                tmem_ld_16x256b_x8(tcol + (16u << 16), fb);
                 tmem_wait_tied<16>(fa);
                 tmem_wait_tied<16>(fa + 16);
+                tmem_ld_16x256b_x8(tcol + (16u << 16), fb);
+                frag_sum(fa, acc[0], acc[1]);
                 tmem_wait_tied<16>(fb);
                 tmem_wait_tied<16>(fb + 16);
                 release();
-                frag_sum(fa, acc[0], acc[1]);
                 frag_sum(fb, acc[2], acc[3]);
               } else {                      // one half at a time (fewer registers)
                 tmem_ld_16x256b_x8(tcol, fa);
