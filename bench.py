@@ -52,6 +52,24 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def reduce_max_over_ranks(value, device):
+    """Max of a per-rank float over the process group: the slowest rank sets
+    the job's time.  Works with any backend (nccl on the GPUs, gloo on CPU)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, steps, max_ms):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time."""
+    return world * units_per_rank * steps / (max_ms / 1e3)
+
+
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -133,26 +151,10 @@ def traffic_record():
 
 
 def oracle_sample_rate(wl, x, n_rows, seed=0):
-    """Queries/s of the CPU oracle on `n_rows` query rows of the workload
-    (uniformly spread positions), including the key-side preprocessing and
-    quantisation the rows need."""
-    import oracle.dsa_oracle as O
-    rng = np.random.default_rng(seed)
-    T = wl.total_tokens
-    rows = np.sort(rng.choice(T, size=n_rows, replace=False))
-    t0 = time.perf_counter()
-    cu = wl.cu_seqlens
-    pos = O.positions_in_document(cu)
-    kk = O.key_layernorm(x["k"], x["ln_gamma"], x["ln_beta"], 1e-6)
-    kk = O.round_fp32(O.apply_rope(kk, pos, wl.rope_dim, wl.rope_base))
-    kq = O.scoring_operand(kk, wl.prec)[0]
-    qrows = O.round_fp32(O.apply_rope(x["q"][rows].astype(np.float64), pos[rows][:, None], wl.rope_dim,
-                                      wl.rope_base))
-    qq = np.zeros((T, wl.n_heads, wl.head_dim))
-    qq[rows] = O.scoring_operand(qrows.reshape(-1, wl.head_dim), wl.prec)[0].reshape(len(rows), wl.n_heads, -1)
-    O.indexer_topk(qq, kq, x["w"].astype(np.float64), cu, wl.index_topk, rows=rows)
-    dt = time.perf_counter() - t0
-    return n_rows / dt, dt, rows
+    """Queries/s of the CPU oracle on min(n_rows, T) query rows of the bench
+    workload in its own precision; returns (rate, seconds, rows timed)."""
+    rate, dt = oracle_rate(wl, x, wl.prec, n_rows, seed)
+    return rate, dt, min(n_rows, wl.total_tokens)
 
 
 def oracle_rate(wl, x, prec, n_rows, seed=0):
@@ -257,12 +259,13 @@ def run_reference(args, wl):
     n_rows = max(8, args.ref_rows // max(1, args.steps))   # the whole run stays within about a minute
     for _ in range(args.warmup):
         oracle_sample_rate(wl, x, max(1, n_rows // 4), seed=99)
-    times, rates = [], []
+    times, done = [], 0
     for s in range(args.steps):
-        rate, dt, _ = oracle_sample_rate(wl, x, n_rows, seed=s)
+        _, dt, rows = oracle_sample_rate(wl, x, n_rows, seed=s)
         times.append(dt)
-        rates.append(rate)
-    value = n_rows * args.steps / sum(times)
+        done += rows
+    n_rows = done // args.steps
+    value = done / sum(times)
     cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": args.gpus,
@@ -352,10 +355,7 @@ def run_native(args, wl):
     sc_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
     step_ms = [a + c for a, c in zip(pre_ms, sc_ms)]
     total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=devn)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_over_ranks(total_ms, devn)
     st = dsa.read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
@@ -417,7 +417,7 @@ def run_native(args, wl):
     e2e_run(e2e_steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / e2e_steps, devn)
     st = dsa.read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after the end-to-end steps")
@@ -453,9 +453,9 @@ def run_native(args, wl):
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     pre_bytes = T * H * D * 4 + T * D * 4 + T * H * D + T * H * D // 32 + T * D + T * D // 32
     tr = traffic_record()
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = job_rate(world, T, args.steps, total_ms)
     cpu_rate, cpu_dt, _ = (None, None, None)
-    if not args.no_cpu:
+    if not args.no_cpu and world == 1:   # the oracle baseline: rank 0 at N = 1 only
         cpu_rate, cpu_dt, _ = oracle_sample_rate(wl, x, args.ref_rows)
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
@@ -477,7 +477,7 @@ def run_native(args, wl):
                      "traffic": tr["bytes_per_launch"] if tr else None,
                      "traffic_source": tr["scaled_to"] if tr else None},
         "bf16_scoring": bf16,
-        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "queries/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_rate(world, T, 1, e2e_ms), "unit": "queries/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host q,k,w -> dsa_idx_preprocess -> dsa_idx_score_topk -> host top-k indices; "
                         "copies on two copy streams overlap the neighbouring steps' compute (two buffer sets)"},
