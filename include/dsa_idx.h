@@ -84,7 +84,10 @@ typedef enum { DSA_MX_SCALE_NOSAT = 0, DSA_MX_SCALE_FLOOR = 1 } dsa_mx_scale_rul
 
 /* dsa_idx_score_topk flags. */
 #define DSA_FLAG_DETERMINISTIC 0x1   /* [P2] deterministic Top-K tie break; always honoured */
-#define DSA_FLAG_SORT_BY_SCORE 0x2   /* rows in (score desc, index asc) order instead of index asc */
+/* Rows in ranking order, score descending then index ascending, instead of
+ * ascending index: the order of the repeated-varlen-ends regression rows in
+ * [P1]'s review ("Preservation and acceptance"). */
+#define DSA_FLAG_SORT_BY_SCORE 0x2
 #define DSA_FLAG_KPOOL_TAIL 0x4      /* [P3] always_select_tail: append the query's incomplete pool */
 /* [P2] compressed keys: kpool_size is the indexer's `ratio` (2..64); k holds
  * caller-computed compressed keys, cu_pools their per-document prefix; each
@@ -216,10 +219,14 @@ dsa_status_t dsa_idx_kpool_compress(
  *               floor(L_d / kpool_size) of them; more are never visible)
  *   topk_idx    device int32 [total_tokens, W] (W = dsa_idx_output_width):
  *               selected local indices in ascending order, then -1
- *               padding (DSA_FLAG_SORT_BY_SCORE is reserved and returns
- *               DSA_ERR_UNSUPPORTED).  KPool mode: the expanded tokens of
- *               the selected pools, then the tail tokens.  Compressed keys:
- *               the selected compressed-key indices (W = index_topk).
+ *               padding; with DSA_FLAG_SORT_BY_SCORE in ranking order
+ *               (score desc, index asc) instead, by a second kernel over
+ *               the finished rows (topk_score is then required: NULL
+ *               returns DSA_ERR_INVALID_ARG).  KPool mode: the expanded
+ *               tokens of the selected pools (pools in the row order above,
+ *               each pool's tokens ascending), then the tail tokens.
+ *               Compressed keys: the selected compressed-key indices
+ *               (W = index_topk).
  *   topk_score  device fp32 [total_tokens, W] or NULL: the score of each
  *               entry (pooled score for pool tokens, +INF for tail tokens,
  *               -INF for padding)

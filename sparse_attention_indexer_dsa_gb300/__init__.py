@@ -156,18 +156,28 @@ def kpool_compress(k: torch.Tensor, gate_bits: torch.Tensor, slot_bias: torch.Te
     return kp, cu_pools
 
 
+def _order_flag(order: str, return_scores: bool = True) -> int:
+    if order not in ("index", "score"):
+        raise ValueError(f"order must be 'index' or 'score', not {order!r}")
+    if order == "score" and not return_scores:
+        raise ValueError("order='score' ranks rows by their scores: return_scores must be True")
+    return DSA_FLAG_SORT_BY_SCORE if order == "score" else 0
+
+
 def score_topk(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: torch.Tensor,
                k_scale: Optional[torch.Tensor], w: torch.Tensor, cu_seqlens: torch.Tensor,
                max_seqlen: int, n_heads: int, index_topk: int, prec="bf16", sm_scale: float = 1.0,
                kpool_size: int = 1, cu_pools: Optional[torch.Tensor] = None, tail: bool = True,
                return_scores: bool = True, ws: Optional[torch.Tensor] = None, out=None,
-               compressed: bool = False):
+               compressed: bool = False, order: str = "index"):
     """Fused score + top-k (dsa_idx_score_topk).
 
     q_op [T*H, D] (bf16 or E4M3 codes), k_op [rows, D], w [T, H] fp32/bf16.
     kpool_size > 1: KPool pools of that size, or with compressed=True the
     compression ratio of caller-provided compressed keys (cu_pools = their
     per-document prefix; indices are reported per compressed key).
+    order "index": each row in ascending index order; "score": score
+    descending, index ascending (KPool tail tokens stay last).
     Returns (idx int32 [T, W], scores fp32 [T, W] or None, lens int32 [T])."""
     T = w.shape[0]
     D = q_op.shape[-1]
@@ -176,6 +186,7 @@ def score_topk(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: torch.
         flags = DSA_FLAG_DETERMINISTIC | DSA_FLAG_COMPRESSED_KEYS
     else:
         flags = DSA_FLAG_DETERMINISTIC | (DSA_FLAG_KPOOL_TAIL if (kpool_size > 1 and tail) else 0)
+    flags |= _order_flag(order, return_scores)
     W = _abi.load().dsa_idx_output_width(index_topk, kpool_size, flags)
     if out is None:
         idx = torch.empty((T, W), dtype=torch.int32, device=q_op.device)
@@ -197,7 +208,7 @@ def score_topk_kv(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: tor
                   k_scale: Optional[torch.Tensor], w: torch.Tensor, cu_seqlens_q: torch.Tensor,
                   cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, n_heads: int,
                   index_topk: int, prec="bf16", sm_scale: float = 1.0, return_scores: bool = True,
-                  ws: Optional[torch.Tensor] = None, out=None):
+                  ws: Optional[torch.Tensor] = None, out=None, order: str = "index"):
     """Fused score + top-k with more keys than queries per document
     (dsa_idx_score_topk_kv): document d's queries are its last T_d tokens.
 
@@ -219,8 +230,8 @@ def score_topk_kv(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: tor
     code = _abi.load().dsa_idx_score_topk_kv(
         _ptr(q_op), _ptr(q_scale), _ptr(k_op), _ptr(k_scale), _ptr(w), _dtype(w), sm_scale,
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Tq, Tk, max_seqlen_q, max_seqlen_k, n_heads, D,
-        index_topk, _prec(prec), DSA_FLAG_DETERMINISTIC, _ptr(idx), _ptr(sc), _ptr(lens), _ptr(ws),
-        ws.numel(), _stream())
+        index_topk, _prec(prec), DSA_FLAG_DETERMINISTIC | _order_flag(order, return_scores), _ptr(idx), _ptr(sc),
+        _ptr(lens), _ptr(ws), ws.numel(), _stream())
     _check(code, "dsa_idx_score_topk_kv")
     return idx, sc, lens
 

@@ -325,8 +325,9 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   if (w_dtype != DSA_DTYPE_F32 && w_dtype != DSA_DTYPE_BF16) return fail(DSA_ERR_INVALID_ARG, "w_dtype");
   if (flags & ~(DSA_FLAG_DETERMINISTIC | DSA_FLAG_SORT_BY_SCORE | DSA_FLAG_KPOOL_TAIL | DSA_FLAG_COMPRESSED_KEYS))
     return fail(DSA_ERR_INVALID_ARG, "unknown flag bits");
-  if (flags & DSA_FLAG_SORT_BY_SCORE) return fail(DSA_ERR_UNSUPPORTED, "DSA_FLAG_SORT_BY_SCORE is not implemented");
   const bool compressed = (flags & DSA_FLAG_COMPRESSED_KEYS) != 0;
+  const bool rank_order = (flags & DSA_FLAG_SORT_BY_SCORE) != 0;
+  if (rank_order && !topk_score) return fail(DSA_ERR_INVALID_ARG, "DSA_FLAG_SORT_BY_SCORE needs topk_score");
   if (kpool_size < 1) return fail(DSA_ERR_INVALID_ARG, "kpool_size");
   if (compressed) {
     if (kpool_size < 2 || kpool_size > 64) return fail(DSA_ERR_UNSUPPORTED, "compression ratio must be 2..64");
@@ -411,6 +412,10 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   if (bound < grid) grid = (int)bound;
   e = launch_score_topk(p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "score_topk launch");
+  if (rank_order) {
+    e = launch_rank_rows(topk_idx, topk_score, total_tokens, p.out_width, di.sm_count, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rank_rows launch");
+  }
   return DSA_OK;
 }
 

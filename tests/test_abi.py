@@ -110,6 +110,11 @@ def test_host_checks_of_the_extended_modes(lib):
     assert rc == _abi.DSA_ERR_UNSUPPORTED
     rc = lib.dsa_idx_quantize_fp8_rows(P(256), 0, 4, 64, 0, P(256), P(256), None)
     assert rc == _abi.DSA_ERR_UNSUPPORTED
+    # ranking order ranks by the scores: topk_score is required
+    rc = lib.dsa_idx_score_topk(P(256), None, P(256), None, P(256), 0, 1.0, P(256), 1, 16, 16, 64, 128,
+                                16, 0, F | _abi.DSA_FLAG_SORT_BY_SCORE, 1, None, P(256), None, None, P(256),
+                                1 << 20, None)
+    assert rc == _abi.DSA_ERR_INVALID_ARG
 
 
 def test_score_plan_fits_every_supported_shape(lib):
