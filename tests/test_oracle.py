@@ -574,3 +574,84 @@ def test_kpool_selection_tail_and_visibility():
             assert blk[0] % P == 0 and (np.diff(blk) == 1).all()
     r2 = O.kpool_topk(q, kbar, w, cu, cp, 8, P, False)
     assert (r2["len"] % P == 0).all()
+
+
+# ----------------------------------------------------------------- ranking order
+
+def _ranked(idx, sc, n):
+    """Entries [0, n) reordered by a plain sort on (score desc, index asc)."""
+    order = sorted(range(n), key=lambda e: (-float(sc[e]), int(idx[e])))
+    return idx[order], sc[order]
+
+
+def test_score_order_ranks_the_index_order_rows():
+    """order="score" holds the same entries as order="index", ranked by their
+    own scores with ties to the lower index (integer scores: many ties)."""
+    rng = np.random.default_rng(801)
+    lens, H, D, k = [40, 1, 23], 4, 8, 9
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q = rng.integers(-2, 3, (T, H, D)).astype(np.float64)
+    kk = rng.integers(-2, 3, (T, D)).astype(np.float64)
+    w = rng.integers(-1, 2, (T, H)).astype(np.float64)
+    a = O.indexer_topk(q, kk, w, cu, k)
+    b = O.indexer_topk(q, kk, w, cu, k, order="score")
+    np.testing.assert_array_equal(a["len"], b["len"])
+    for r in range(T):
+        n = int(a["len"][r])
+        assert (np.diff(a["idx"][r, :n]) > 0).all()
+        ri, rs = _ranked(a["idx"][r], a["score"][r], n)
+        np.testing.assert_array_equal(b["idx"][r, :n], ri)
+        np.testing.assert_array_equal(b["score"][r, :n], rs)
+        assert (b["idx"][r, n:] == -1).all()
+        if n:   # the first entry is the best visible key (brute force)
+            s = O.indexer_scores(q[r], kk[cu[np.searchsorted(cu, r, side="right") - 1]:r + 1], w[r])
+            assert b["score"][r, 0] == s.max() and b["idx"][r, 0] == int(np.flatnonzero(s == s.max())[0])
+
+
+@pytest.mark.parametrize("P,tail", [(4, True), (2, False)])
+def test_kpool_score_order_ranks_pools_and_keeps_the_tail_last(P, tail):
+    rng = np.random.default_rng(802 + P)
+    lens, H, D, k = [37, 6], 4, 8, 4 * P
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    npool = [L // P for L in lens]
+    cp = np.concatenate([[0], np.cumsum(npool)])
+    q = rng.integers(-2, 3, (T, H, D)).astype(np.float64)
+    kb = rng.integers(-2, 3, (sum(npool), D)).astype(np.float64)
+    w = rng.integers(-1, 2, (T, H)).astype(np.float64)
+    a = O.kpool_topk(q, kb, w, cu, cp, k, P, tail)
+    b = O.kpool_topk(q, kb, w, cu, cp, k, P, tail, order="score")
+    np.testing.assert_array_equal(a["len"], b["len"])
+    for r in range(T):
+        n = int(a["len"][r])
+        ntail = int(np.sum(np.isposinf(a["score"][r, :n])))
+        npt = n - ntail
+        # pools: groups of P consecutive tokens, ranked by (score desc, pool asc)
+        pa = a["idx"][r, :npt].reshape(-1, P)[:, 0] // P
+        sa = a["score"][r, :npt].reshape(-1, P)[:, 0]
+        rp, _ = _ranked(pa, sa, len(pa))
+        exp = (rp[:, None] * P + np.arange(P)[None, :]).reshape(-1)
+        np.testing.assert_array_equal(b["idx"][r, :npt], exp)
+        # the tail: unchanged, last
+        np.testing.assert_array_equal(b["idx"][r, npt:n], a["idx"][r, npt:n])
+        assert np.isposinf(b["score"][r, npt:n]).all()
+
+
+def test_compressed_score_order_ranks_the_index_order_rows():
+    rng = np.random.default_rng(803)
+    lens, H, D, k, ratio = [50, 9], 4, 8, 5, 4
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    nc = [L // ratio for L in lens]
+    cc = np.concatenate([[0], np.cumsum(nc)])
+    q = rng.integers(-2, 3, (T, H, D)).astype(np.float64)
+    kc = rng.integers(-2, 3, (sum(nc), D)).astype(np.float64)
+    w = rng.integers(-1, 2, (T, H)).astype(np.float64)
+    a = O.compressed_topk(q, kc, w, cu, cc, k, ratio)
+    b = O.compressed_topk(q, kc, w, cu, cc, k, ratio, order="score")
+    for r in range(T):
+        n = int(a["len"][r])
+        ri, rs = _ranked(a["idx"][r], a["score"][r], n)
+        np.testing.assert_array_equal(b["idx"][r, :n], ri)
+        np.testing.assert_array_equal(b["score"][r, :n], rs)
