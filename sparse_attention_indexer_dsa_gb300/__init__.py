@@ -212,9 +212,9 @@ def score_topk_kv(q_op: torch.Tensor, q_scale: Optional[torch.Tensor], k_op: tor
     """Fused score + top-k with more keys than queries per document
     (dsa_idx_score_topk_kv): document d's queries are its last T_d tokens.
 
-    q_op [Tq*H, D], k_op [Tk, D], w [Tq, H].  Returns (idx int32 [Tq, k],
-    scores fp32 [Tq, k] or None, lens int32 [Tq]); indices are local to the
-    document's keys."""
+    q_op [Tq*H, D], k_op [Tk, D], w [Tq, H].  order as in score_topk.
+    Returns (idx int32 [Tq, k], scores fp32 [Tq, k] or None, lens int32
+    [Tq]); indices are local to the document's keys."""
     Tq, Tk = w.shape[0], k_op.shape[0]
     D = q_op.shape[-1]
     B = cu_seqlens_q.numel() - 1
