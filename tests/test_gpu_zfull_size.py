@@ -1,0 +1,97 @@
+"""Parity at the full sizes of the measured configurations, in the launch
+configuration bench.py times: the seeded inputs resident on the device,
+dsa_idx_preprocess (key LayerNorm, RoPE, quantisation; KPool: pool
+compression) and the fused score + top-k over every query, then sampled rows
+checked against the oracle, which computes them one by one from the same
+seeded inputs: the first two and last two queries of every document and a
+seeded spread."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.dsa_oracle as O
+import sparse_attention_indexer_dsa_gb300 as dsa
+from sparse_attention_indexer_dsa_gb300 import workloads as W
+from tests.gpu_util import dev, host
+from tests.parity import REL_BF16, REL_MXFP8, compare_topk
+
+pytestmark = pytest.mark.gpu
+
+CASES = [("c3", "mxfp8"), ("c3", "bf16"), ("thd", "mxfp8"), ("kpool", "bf16"), ("target", "mxfp8"),
+         ("target", "bf16"), ("target", "fp8")]
+
+
+def sample_rows(wl, n_spread=24, seed=0):
+    cu = wl.cu_seqlens
+    rows = []
+    for d in range(len(wl.doc_lens)):
+        a, b = int(cu[d]), int(cu[d + 1])
+        rows += [r for r in (a, a + 1, b - 2, b - 1) if a <= r < b]
+    rows += np.random.default_rng(seed).choice(wl.total_tokens, n_spread, replace=False).tolist()
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def oracle_rows(wl, x, prec, rows):
+    """The oracle's preprocessing and selection for the sampled query rows
+    (a query's RoPE and quantisation depend on its own row only; the keys are
+    processed whole)."""
+    T, H, D = wl.total_tokens, wl.n_heads, wl.head_dim
+    cu = wl.cu_seqlens
+    pos = O.positions_in_document(cu)
+    kk = np.asarray(x["k"], np.float64)
+    if wl.layernorm:
+        kk = O.key_layernorm(kk, x["ln_gamma"], x["ln_beta"], 1e-6)
+    kf = O.round_fp32(O.apply_rope(kk, pos, wl.rope_dim, wl.rope_base))
+    qf = O.round_fp32(O.apply_rope(np.asarray(x["q"][rows], np.float64), pos[rows][:, None], wl.rope_dim,
+                                   wl.rope_base))
+    qq = np.zeros((T, H, D))
+    w = x["w"].astype(np.float64)
+    if wl.kpool > 1:
+        kbar, cpools = O.kpool_compress(x["k"], O.bf16_bits_to_float(x["gate_bits"]), x["slot_bias"], cu, wl.kpool)
+        qq[rows] = O.round_bf16(qf)
+        return O.kpool_topk(qq, O.round_bf16(kbar), w, cu, cpools, wl.index_topk, wl.kpool, True, rows=rows,
+                            with_scale=True)
+    qq[rows] = O.scoring_operand(qf.reshape(-1, D), prec)[0].reshape(len(rows), H, D)
+    return O.indexer_topk(qq, O.scoring_operand(kf, prec)[0], w, cu, wl.index_topk, rows=rows, with_scale=True)
+
+
+def rel_for(prec):
+    # the two preprocessing chains round to FP32 independently, which can move a
+    # scoring operand by one step of its format (BF16: one ulp; E4M3: absorbed)
+    return REL_BF16 + 2.0 ** -8 if prec == "bf16" else REL_MXFP8
+
+
+@pytest.mark.parametrize("name,prec", CASES, ids=[f"{n}-{p}" for n, p in CASES])
+def test_full_size_sampled_rows(name, prec):
+    wl = W.config(name)
+    x = W.make_inputs(wl)
+    T, H, D, K = wl.total_tokens, wl.n_heads, wl.head_dim, wl.index_topk
+    cu = dev(wl.cu_seqlens)
+    k = dev(x["k"])
+    g = dev(x["ln_gamma"]) if wl.layernorm else None
+    b = dev(x["ln_beta"]) if wl.layernorm else None
+    qo, qs, ko, ks = dsa.preprocess(dev(x["q"]), k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base,
+                                    False, True, prec)
+    pool = {}
+    if wl.kpool > 1:
+        ko, cpools = dsa.kpool_compress(k, dev(x["gate_bits"].view(np.int16)), dev(x["slot_bias"]), cu, wl.kpool)
+        ks = None
+        pool = dict(kpool_size=wl.kpool, cu_pools=cpools, tail=True)
+    ws = dsa.workspace(T, len(wl.doc_lens), wl.max_seqlen, H, D, K, wl.kpool, prec, qo.device)
+    idx, sc, ln = dsa.score_topk(qo, qs, ko, ks, dev(x["w"]), cu, wl.max_seqlen, H, K, prec, ws=ws, **pool)
+    assert dsa.read_status(ws) == 0
+    gi, gs, gl = host(idx), host(sc), host(ln)
+    del qo, qs, ko, ks, idx, sc, ln
+    torch.cuda.empty_cache()
+    # every row: lengths and padding follow from the visibility rule alone
+    pos = O.positions_in_document(wl.cu_seqlens)
+    if wl.kpool > 1:
+        P = wl.kpool
+        exp_len = np.minimum((pos + 1) // P, K // P) * P + (pos + 1) % P
+    else:
+        exp_len = np.minimum(pos + 1, K)
+    np.testing.assert_array_equal(gl, exp_len)
+    assert all((gi[t, gl[t]:] == -1).all() for t in range(0, T, 97))
+    rows = sample_rows(wl)
+    ref = oracle_rows(wl, x, prec, rows)
+    compare_topk(gi, gs, gl, ref, rel_for(prec), pool=wl.kpool, tail=True, rows=rows)
