@@ -50,3 +50,23 @@ def test_job_rate_formula():
     import bench
     assert bench.job_rate(1, 32768, 10, 70.0) == 32768 * 10 / 0.070
     assert bench.job_rate(8, 32768, 10, 70.0) == 8 * bench.job_rate(1, 32768, 10, 70.0)
+
+
+def test_reference_arm_line_keeps_the_contract():
+    """One process: the reference arm's JSON line carries every key of the
+    bench contract (the oracle timed on the host cores)."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "1",
+                        "--workload", "tiny", "--ref-rows", "16"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300, env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = lines[0]
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["higher_is_better"] is True
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None and "workload" in d["config"]
+    assert set(d["cpu_baseline"]) >= {"value", "unit", "cores", "kind", "sample"}
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert abs(d["ms_per_step"] * d["steps"] / 1e3 * d["value"] - 2 * 8) < 1e-6 * d["value"] + 1e-6
