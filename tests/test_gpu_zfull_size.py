@@ -61,9 +61,16 @@ def rel_for(prec):
     return REL_BF16 + 2.0 ** -8 if prec == "bf16" else REL_MXFP8
 
 
-@pytest.mark.parametrize("name,prec", CASES, ids=[f"{n}-{p}" for n, p in CASES])
+MAX_LEN = W.Workload("max-seqlen", [65536], 16, 128, 2048, "mxfp8", "normal", layernorm=True, rope_dim=64,
+                     rope_fp32=True, w_std=0.25, seed=1009)
+
+
+@pytest.mark.parametrize("name,prec", CASES + [("max-seqlen", "mxfp8")],
+                         ids=[f"{n}-{p}" for n, p in CASES] + ["max-seqlen-mxfp8"])
 def test_full_size_sampled_rows(name, prec):
-    wl = W.config(name)
+    """The measured configurations, and one document of the longest supported
+    length (65536 tokens: local indices up to 65535, 512 key tiles)."""
+    wl = MAX_LEN if name == "max-seqlen" else W.config(name)
     x = W.make_inputs(wl)
     T, H, D, K = wl.total_tokens, wl.n_heads, wl.head_dim, wl.index_topk
     cu = dev(wl.cu_seqlens)
