@@ -2,15 +2,17 @@
 // descending, index ascending, the order of the repeated-varlen-ends rows in
 // PR #8403's review ("Preservation and acceptance").  A pass over the rows
 // the fused kernel wrote, so the fused kernel itself is the same in either
-// order.  One CTA of 128 threads per row (grid-stride): the row's rankable
+// order.  One CTA of 128 threads per row (grid-stride).  The row's rankable
 // prefix (valid entries with a finite score; KPool tail tokens, scored +INF,
-// stay last) is packed as (order-preserving score key << 16) | (0xFFFF -
-// index), sorted by a bitonic network held in registers (E consecutive slots
-// a thread; pairs closer than E slots in registers, closer than 32 E by warp
-// shuffles, the rest through shared memory), and written back.  Indices are
-// below 65536 in every mode, and the fused kernel writes canonical scores
-// (-0 as +0), so the round trip through the key is exact.  Bandwidth-bound:
-// each row is read and written once.
+// stay last) arrives in ascending index order, so a stable sort on the
+// order-preserving 32-bit score key alone gives the ranking: a block radix
+// sort, least significant 4-bit digit first, E entries a thread, skipping
+// the digits on which every entry agrees.  Per digit: each thread counts its
+// entries in its own column of a digit-major counter table, one block scan
+// turns the counts into destinations, and the entries are scattered through
+// shared memory (slot index padded by one per 32, conflict-free).  Indices
+// are below 65536 in every mode, and the fused kernel writes canonical scores
+// (-0 as +0), so the round trip through the key is exact.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,8 +23,9 @@ namespace {
 
 constexpr int kRankThreads = 128;
 constexpr int kRankMaxSlots = 2048;   // index_topk <= 2048 entries carry a finite score
+constexpr int kDigits = 16;           // 4-bit digits
 
-__device__ __forceinline__ int padded(int g) { return g + (g >> 5); }   // conflict-free strided slots
+__device__ __forceinline__ int padded(int g) { return g + (g >> 5); }
 
 __device__ __forceinline__ uint32_t score_key(float v) {
   uint32_t b = __float_as_uint(v);
@@ -34,115 +37,134 @@ __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
-__device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+struct RankSmem {
+  uint32_t key[kRankMaxSlots + kRankMaxSlots / 32];
+  uint16_t idx[kRankMaxSlots + kRankMaxSlots / 32];
+  uint32_t cnt[kDigits * kRankThreads + kDigits * kRankThreads / 32];   // digit-major, padded
+  uint32_t red[8];
+  int n;
+};
 
-// One network stage between slots J apart inside a thread (J < E).
-template <int J, int E>
-__device__ __forceinline__ void stage_in_thread(uint64_t (&c)[E], int tid, int k2) {
-  if constexpr (J < E) {
+// Sorts entries 0 .. n-1 of sm (padded slots; entries n .. 128E-1 hold key 0,
+// index 0xFFFF) by key descending, stably.  Thread t holds entries tE .. tE+E-1.
+template <int E>
+__device__ __forceinline__ void rank_sort(RankSmem& sm, int n, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t key[E], idx[E];
+  uint32_t vor = 0u, vand = 0xFFFFFFFFu;   // over the real entries only
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int g = tid * E + e;
+    key[e] = sm.key[padded(g)];
+    idx[e] = sm.idx[padded(g)];
+    if (g < n) {
+      vor |= key[e];
+      vand &= key[e];
+    }
+  }
+  vor = __reduce_or_sync(0xffffffffu, vor);
+  vand = __reduce_and_sync(0xffffffffu, vand);
+  if (lane == 0) {
+    sm.red[warp] = vor;
+    sm.red[4 + warp] = vand;
+  }
+  __syncthreads();
+  const uint32_t vary = (sm.red[0] | sm.red[1] | sm.red[2] | sm.red[3]) ^
+                        (sm.red[4] & sm.red[5] & sm.red[6] & sm.red[7]);
+  __syncthreads();   // red is reused by the scans
+#pragma unroll 1
+  for (int shift = 0; shift < 32; shift += 4) {
+    if (((vary >> shift) & 0xFu) == 0u) continue;   // every entry has the same digit: order kept
+    // 1. count: digit' = 15 - digit (descending keys), rank among this thread's earlier entries
+#pragma unroll
+    for (int d = 0; d < kDigits; ++d) sm.cnt[padded(d * kRankThreads + tid)] = 0u;
+    uint32_t dg[E], rk[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      if ((e & J) == 0) {
-        const bool best_first = ((tid * E + e) & k2) == 0;
-        const uint64_t a = c[e], b = c[e | J];
-        c[e] = best_first ? umax64(a, b) : umin64(a, b);
-        c[e | J] = best_first ? umin64(a, b) : umax64(a, b);
-      }
+      dg[e] = 15u - ((key[e] >> shift) & 0xFu);
+      const int c = padded((int)dg[e] * kRankThreads + tid);
+      rk[e] = sm.cnt[c];
+      sm.cnt[c] = rk[e] + 1u;
     }
+    __syncthreads();
+    // 2. exclusive scan of the counters in digit-major order; thread t owns
+    //    linear positions 16t .. 16t+15
+    uint32_t v[kDigits], tot = 0u;
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i) {
+      v[i] = sm.cnt[padded(kDigits * tid + i)];
+      tot += v[i];
+    }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm.red[warp] = incl;
+    __syncthreads();
+    uint32_t base = incl - tot;
+    for (int w = 0; w < warp; ++w) base += sm.red[w];
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i) {
+      sm.cnt[padded(kDigits * tid + i)] = base;
+      base += v[i];
+    }
+    __syncthreads();
+    // 3. scatter to the destinations, then reload in thread order
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int dst = (int)(sm.cnt[padded((int)dg[e] * kRankThreads + tid)] + rk[e]);
+      sm.key[padded(dst)] = key[e];
+      sm.idx[padded(dst)] = (uint16_t)idx[e];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      key[e] = sm.key[padded(tid * E + e)];
+      idx[e] = sm.idx[padded(tid * E + e)];
+    }
+    __syncthreads();   // every reload (and every read of cnt) before the next digit's writes
   }
 }
 
-// Sorts the NP = 128 E packed entries at padded slots of sm descending, in
-// place.  The stage loops stay rolled (a fully unrolled network overflows the
-// instruction cache); only the per-slot loops unroll.
-template <int E>
-__device__ __forceinline__ void rank_sort(uint64_t* sm, int tid) {
-  constexpr int NP = kRankThreads * E;
-  uint64_t c[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) c[e] = sm[padded(tid * E + e)];
-  __syncthreads();
-#pragma unroll 1
-  for (int k2 = 2; k2 <= NP; k2 <<= 1) {
-#pragma unroll 1
-    for (int j = k2 >> 1; j > 0; j >>= 1) {
-      if (j < E) {                                  // both slots in this thread
-        switch (j) {
-          case 1: stage_in_thread<1, E>(c, tid, k2); break;
-          case 2: stage_in_thread<2, E>(c, tid, k2); break;
-          case 4: stage_in_thread<4, E>(c, tid, k2); break;
-          default: stage_in_thread<8, E>(c, tid, k2); break;
-        }
-        continue;
-      }
-      const int m = j / E;                          // partner thread: tid ^ m
-      const bool lower = (tid & m) == 0;
-      if (j < 32 * E) {                             // same warp
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)c[e], m);
-          const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(c[e] >> 32), m);
-          const uint64_t o = ((uint64_t)hi << 32) | lo;
-          const bool best_first = (((tid * E + e) & ~j) & k2) == 0;
-          c[e] = (lower == best_first) ? umax64(c[e], o) : umin64(c[e], o);
-        }
-      } else {                                      // another warp
-#pragma unroll
-        for (int e = 0; e < E; ++e) sm[padded(tid * E + e)] = c[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const uint64_t o = sm[padded((tid * E + e) ^ j)];
-          const bool best_first = (((tid * E + e) & ~j) & k2) == 0;
-          c[e] = (lower == best_first) ? umax64(c[e], o) : umin64(c[e], o);
-        }
-        __syncthreads();
-      }
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < E; ++e) sm[padded(tid * E + e)] = c[e];
-  __syncthreads();
-}
-
-__global__ void __launch_bounds__(kRankThreads, 4) rank_rows_kernel(int32_t* idx, float* score, int64_t rows,
+__global__ void __launch_bounds__(kRankThreads) rank_rows_kernel(int32_t* idx, float* score, int64_t rows,
                                                                   int width) {
-  __shared__ uint64_t sm[kRankMaxSlots + kRankMaxSlots / 32];
-  __shared__ int s_n;
+  __shared__ RankSmem sm;
   const int tid = threadIdx.x;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     int32_t* ri = idx + r * width;
     float* rs = score + r * width;
-    if (tid == 0) s_n = 0;
+    if (tid == 0) sm.n = 0;
     __syncthreads();
     // the rankable entries are a prefix of the row: valid (index >= 0) with a finite score
     int last = 0;
     for (int g = tid; g < width; g += kRankThreads)
       if (ri[g] >= 0 && rs[g] != __int_as_float(0x7f800000)) last = g + 1;
-    if (last > 0) atomicMax(&s_n, last);
+    if (last > 0) atomicMax(&sm.n, last);
     __syncthreads();
-    const int n = s_n < kRankMaxSlots ? s_n : kRankMaxSlots;
+    const int n = sm.n < kRankMaxSlots ? sm.n : kRankMaxSlots;
     if (n > 1) {
       int np = kRankThreads;
       while (np < n) np <<= 1;
-      for (int g = tid; g < np; g += kRankThreads)
-        sm[padded(g)] = g < n ? ((uint64_t)score_key(rs[g]) << 16) | (uint64_t)(0xFFFFu - (uint32_t)ri[g]) : 0ull;
+      for (int g = tid; g < np; g += kRankThreads) {
+        sm.key[padded(g)] = g < n ? score_key(rs[g]) : 0u;
+        sm.idx[padded(g)] = g < n ? (uint16_t)ri[g] : (uint16_t)0xFFFFu;
+      }
       __syncthreads();
       switch (np / kRankThreads) {
-        case 1: rank_sort<1>(sm, tid); break;
-        case 2: rank_sort<2>(sm, tid); break;
-        case 4: rank_sort<4>(sm, tid); break;
-        case 8: rank_sort<8>(sm, tid); break;
-        default: rank_sort<16>(sm, tid); break;
+        case 1: rank_sort<1>(sm, n, tid); break;
+        case 2: rank_sort<2>(sm, n, tid); break;
+        case 4: rank_sort<4>(sm, n, tid); break;
+        case 8: rank_sort<8>(sm, n, tid); break;
+        default: rank_sort<16>(sm, n, tid); break;
       }
       for (int g = tid; g < n; g += kRankThreads) {
-        const uint64_t v = sm[padded(g)];
-        ri[g] = (int32_t)(0xFFFFu - (uint32_t)(v & 0xFFFFu));
-        rs[g] = key_score((uint32_t)(v >> 16));
+        ri[g] = (int32_t)sm.idx[padded(g)];
+        rs[g] = key_score(sm.key[padded(g)]);
       }
     }
-    __syncthreads();   // s_n and sm are reused by the next row
+    __syncthreads();   // n and the slots are reused by the next row
   }
 }
 
