@@ -177,6 +177,28 @@ def mx_block_exponent(amax: float, rule: str = "nosat") -> int:
     return int(min(max(e, -UE8M0_BIAS), UE8M0_BIAS))
 
 
+def mx_block_exponents(amax, rule: str = "nosat") -> np.ndarray:
+    """mx_block_exponent applied to every element of the array `amax`, the
+    same search written over arrays: start below the answer (floor(log2 amax)
+    - 10 for "nosat") and step e up while amax > 448 * 2^e, with exact float64
+    comparisons; clamp to [-127, 127]; amax = 0 gives -127."""
+    a = np.asarray(amax, dtype=np.float64)
+    pos = a > 0
+    _, e2 = np.frexp(np.where(pos, a, 1.0))
+    fl = e2.astype(np.int64) - 1                 # floor(log2 amax)
+    if rule == "floor":
+        e = fl - 8
+    else:
+        e = fl - 10
+        while True:
+            up = pos & (a > E4M3_MAX * np.ldexp(1.0, e))
+            if not up.any():
+                break
+            e = e + up
+    e = np.where(pos, e, -UE8M0_BIAS)
+    return np.clip(e, -UE8M0_BIAS, UE8M0_BIAS).astype(np.int64)
+
+
 def quantize_mxfp8(x, rule: str = "nosat") -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """Quantise rows of x [..., D] (D a multiple of 32) to MXFP8.
 
@@ -190,7 +212,7 @@ def quantize_mxfp8(x, rule: str = "nosat") -> Tuple[np.ndarray, np.ndarray, np.n
     assert D % MX_BLOCK == 0
     xb = x.reshape(-1, D // MX_BLOCK, MX_BLOCK)
     amax = np.abs(xb).max(axis=-1)
-    e = np.vectorize(lambda a: mx_block_exponent(float(a), rule), otypes=[np.int64])(amax)
+    e = mx_block_exponents(amax, rule)
     scale = np.ldexp(1.0, e)[..., None]
     payload = round_e4m3_sat(xb / scale)
     deq = (payload * scale).reshape(x.shape)
@@ -211,7 +233,7 @@ def quantize_fp8_rows(x, rule: str = "nosat") -> Tuple[np.ndarray, np.ndarray, n
     D = x.shape[-1]
     xr = x.reshape(-1, D)
     amax = np.abs(xr).max(axis=-1)
-    e = np.vectorize(lambda a: mx_block_exponent(float(a), rule), otypes=[np.int64])(amax)
+    e = mx_block_exponents(amax, rule)
     scale = np.ldexp(1.0, e)[:, None]
     payload = round_e4m3_sat(xr / scale)
     deq = (payload * scale).reshape(x.shape)
@@ -228,6 +250,14 @@ def dequantize_mxfp8(codes, scale_bytes) -> np.ndarray:
     vals = e4m3_decode(codes).reshape(-1, D // MX_BLOCK, MX_BLOCK)
     scale = np.ldexp(1.0, sb.reshape(-1, D // MX_BLOCK) - UE8M0_BIAS)[..., None]
     return (vals * scale).reshape(codes.shape)
+
+
+def dequantize_fp8_rows(codes, scale_bytes) -> np.ndarray:
+    """float64 value of per-vector FP8 data: e4m3_decode(code) * 2^(byte - 127)
+    with one scale byte per row."""
+    codes = np.asarray(codes)
+    sb = np.asarray(scale_bytes, dtype=np.int64)
+    return e4m3_decode(codes) * np.ldexp(1.0, sb - UE8M0_BIAS)[..., None]
 
 
 # ---------------------------------------------------------------------------
@@ -343,6 +373,14 @@ def error_scale(q_t, k_vis, w_t, sm_scale: float = 1.0) -> np.ndarray:
     return abs(sm_scale) * (np.abs(np.asarray(w_t, np.float64)) @ acc)
 
 
+def relu_magnitude(q_t, k_vis, w_t, sm_scale: float = 1.0) -> np.ndarray:
+    """M[s] = |sm_scale| * sum_j |w_t[j]| * max(q_t[j] . k_vis[s], 0): the sum
+    of the magnitudes of the terms the score adds up (|I[s]| <= M[s] <= A[s]).
+    Relative score tolerances are measured against it."""
+    acc = np.asarray(q_t, np.float64) @ np.asarray(k_vis, np.float64).T   # [H, n]
+    return abs(sm_scale) * (np.abs(np.asarray(w_t, np.float64)) @ np.maximum(acc, 0.0))
+
+
 def select_topk(scores, k: int) -> np.ndarray:
     """Indices of the min(k, n) best entries under the total order (score
     descending, index ascending); -0 and +0 are equal.  Returned in that
@@ -379,8 +417,8 @@ def indexer_topk(q_op, k_op, w, cu_seqlens, index_topk: int, sm_scale: float = 1
     k visible keys -> -1 / -inf padding and len = p + 1.  order "index":
     ascending index (the library's default row order); "score": (score desc,
     index asc).  Returns dict(rows, idx [R, k], score [R, k], len [R], and
-    when with_scale all_scores / all_scales: lists of the full score and
-    error-scale rows).
+    when with_scale all_scores / all_scales / all_mags: lists of the full
+    score, error-scale A and ReLU-magnitude M rows).
     """
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     cuk = cu if cu_seqlens_k is None else np.asarray(cu_seqlens_k, dtype=np.int64)
@@ -391,7 +429,7 @@ def indexer_topk(q_op, k_op, w, cu_seqlens, index_topk: int, sm_scale: float = 1
     out_idx = np.full((R, index_topk), -1, dtype=np.int64)
     out_sc = np.full((R, index_topk), -np.inf)
     out_len = np.zeros(R, dtype=np.int64)
-    all_scores, all_scales = [], []
+    all_scores, all_scales, all_mags = [], [], []
     for r, (t, d) in enumerate(zip(rows, doc_of)):
         a = cu[d]
         off = (cuk[d + 1] - cuk[d]) - (cu[d + 1] - cu[d])
@@ -404,11 +442,13 @@ def indexer_topk(q_op, k_op, w, cu_seqlens, index_topk: int, sm_scale: float = 1
         if with_scale:
             all_scores.append(s)
             all_scales.append(error_scale(q_op[t], kv, w[t], sm_scale))
+            all_mags.append(relu_magnitude(q_op[t], kv, w[t], sm_scale))
         assert p + 1 == len(s)
     res = dict(rows=rows, idx=out_idx, score=out_sc, len=out_len)
     if with_scale:
         res["all_scores"] = all_scores
         res["all_scales"] = all_scales
+        res["all_mags"] = all_mags
     return res
 
 
@@ -466,7 +506,7 @@ def compressed_topk(q_op, kc_op, w, cu_seqlens, cu_comp, index_topk: int, ratio:
     out_idx = np.full((R, index_topk), -1, dtype=np.int64)
     out_sc = np.full((R, index_topk), -np.inf)
     out_len = np.zeros(R, dtype=np.int64)
-    all_scores, all_scales = [], []
+    all_scores, all_scales, all_mags = [], [], []
     for r, (t, d) in enumerate(zip(rows, doc_of)):
         p = t - cu[d]
         nvis = (p + 1) // ratio
@@ -477,10 +517,12 @@ def compressed_topk(q_op, kc_op, w, cu_seqlens, cu_comp, index_topk: int, ratio:
         if with_scale:
             all_scores.append(s)
             all_scales.append(error_scale(q_op[t], kv, w[t], sm_scale))
+            all_mags.append(relu_magnitude(q_op[t], kv, w[t], sm_scale))
     res = dict(rows=rows, idx=out_idx, score=out_sc, len=out_len)
     if with_scale:
         res["all_scores"] = all_scores
         res["all_scales"] = all_scales
+        res["all_mags"] = all_mags
     return res
 
 
@@ -511,7 +553,7 @@ def kpool_topk(q_op, kbar_op, w, cu_seqlens, cu_pools, index_topk: int, pool_siz
     out_idx = np.full((R, width), -1, dtype=np.int64)
     out_sc = np.full((R, width), -np.inf)
     out_len = np.zeros(R, dtype=np.int64)
-    all_scores, all_scales = [], []
+    all_scores, all_scales, all_mags = [], [], []
     for r, (t, d) in enumerate(zip(rows, doc_of)):
         p = t - cu[d]
         nvis = (p + 1) // P
@@ -534,8 +576,10 @@ def kpool_topk(q_op, kbar_op, w, cu_seqlens, cu_pools, index_topk: int, pool_siz
         if with_scale:
             all_scores.append(s)
             all_scales.append(error_scale(q_op[t], kv, w[t], sm_scale))
+            all_mags.append(relu_magnitude(q_op[t], kv, w[t], sm_scale))
     res = dict(rows=rows, idx=out_idx, score=out_sc, len=out_len)
     if with_scale:
         res["all_scores"] = all_scores
         res["all_scales"] = all_scales
+        res["all_mags"] = all_mags
     return res

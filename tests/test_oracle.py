@@ -281,6 +281,75 @@ def test_scores_brute_force():
     assert (np.abs(O.indexer_scores(q, k, w, 0.7)) <= A + 1e-12).all()
 
 
+def test_relu_magnitude_brute_force_and_bounds():
+    """M[s] = |sm| sum_j |w_j| max(q_j . k_s, 0), against a plain triple loop;
+    |I| <= M <= A on random rows, and M == |I| when every weight is positive."""
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal((4, 6))
+    k = rng.standard_normal((7, 6))
+    w = rng.standard_normal(4)
+    M = O.relu_magnitude(q, k, w, -0.6)
+    brute = [0.6 * sum(abs(w[j]) * max(sum(q[j, d] * k[s, d] for d in range(6)), 0.0) for j in range(4))
+             for s in range(7)]
+    np.testing.assert_allclose(M, brute, rtol=1e-12)
+    I = O.indexer_scores(q, k, w, -0.6)
+    A = O.error_scale(q, k, w, -0.6)
+    assert (np.abs(I) <= M + 1e-12).all() and (M <= A + 1e-12).all()
+    wp = np.abs(w)
+    np.testing.assert_allclose(O.relu_magnitude(q, k, wp, 0.6), O.indexer_scores(q, k, wp, 0.6), rtol=1e-12)
+    res = O.indexer_topk(q[None].repeat(3, 0), k[:3], w[None].repeat(3, 0), [0, 3], 2, with_scale=True)
+    np.testing.assert_allclose(res["all_mags"][2], O.relu_magnitude(q, k[:3], w), rtol=1e-12)
+
+
+def test_mx_block_exponents_equal_the_scalar_search():
+    """The array form of the block-exponent search gives the scalar search's
+    exponent for every value: zero, subnormals, exact binade edges 448 * 2^e
+    and their neighbours, the UE8M0 clamp at both ends, and random values."""
+    rng = np.random.default_rng(16)
+    edges = [0.0, 5e-324, 2.0 ** -140, 2.0 ** -127 * 448, 2.0 ** 127 * 448, 3.4e38, 1e300]
+    for e in range(-130, 130, 7):
+        b = 448.0 * 2.0 ** e
+        edges += [b, np.nextafter(b, 0), np.nextafter(b, np.inf)]
+    vals = np.concatenate([edges, np.abs(rng.standard_normal(2000)) * np.exp2(rng.integers(-140, 140, 2000))])
+    for rule in ("nosat", "floor"):
+        got = O.mx_block_exponents(vals, rule)
+        want = [O.mx_block_exponent(float(v), rule) for v in vals]
+        np.testing.assert_array_equal(got, want)
+
+
+def test_fp8_rows_dequantisation_round_trip():
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((9, 128)) * np.exp2(rng.integers(-20, 20, (9, 1)))
+    codes, sb, deq = O.quantize_fp8_rows(x)
+    np.testing.assert_array_equal(O.dequantize_fp8_rows(codes, sb), deq)
+    # one byte per row: a row scaled by 2^m dequantises to the scaled values
+    c2, s2, d2 = O.quantize_fp8_rows(x * 8.0)
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(s2.astype(int), sb.astype(int) + 3)
+    np.testing.assert_array_equal(O.dequantize_fp8_rows(c2, s2), deq * 8.0)
+
+
+def test_preprocess_bf16_path_query_closed_form():
+    """Default (rope_fp32 = 0) chain, query side: a query whose rotary pair
+    (0, 32) is the unit vector (1, 0) becomes (cos(p), sin(p)) at position p
+    (theta_0 = 1), rounded once to BF16 (torch's cast of the float64 cosine
+    and sine); the NoPE half comes out as its own BF16 rounding; position 0
+    leaves the rotary dims unrotated."""
+    T, H, D = 7, 1, 128
+    q = np.zeros((T, H, D), np.float32)
+    q[:, 0, 0] = 1.0
+    q[:, 0, 64:] = np.linspace(-3.3, 3.7, 64, dtype=np.float32)
+    k = np.ones((T, D), np.float32)
+    cu = np.array([0, T])
+    qb, _ = O.preprocess(q, k, cu, None, None, 1e-6, 64, 10000.0, False, rope_fp32=False)
+    to_bf16 = lambda v: torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).double().numpy()
+    for p in range(T):
+        assert qb[p, 0, 0] == to_bf16(math.cos(p))
+        assert qb[p, 0, 32] == to_bf16(math.sin(p))
+        np.testing.assert_array_equal(qb[p, 0, 64:], to_bf16(q[p, 0, 64:].astype(np.float64)))
+    assert qb[0, 0, 0] == 1.0 and qb[0, 0, 32] == 0.0
+
+
 def test_golden_bf16_scoring_boundary():
     g = _golden("bf16_scoring_boundary.json")
     q = np.array([[g["q"]]])
