@@ -54,8 +54,9 @@ def test_kpool_workload_end_to_end():
     rows = np.concatenate([np.arange(0, 64), np.arange(2900, 3010), np.arange(T - 40, T)])
     ref = O.kpool_topk(O.bf16_bits_to_float(qb).reshape(T, H, D), O.round_bf16(kbar), x["w"].astype(np.float64),
                        wl.cu_seqlens, rcp, wl.index_topk, P, True, rows=rows, with_scale=True)
-    # pooled keys differ by at most one BF16 ulp between the two sides
-    compare_topk(host(idx), host(sc), host(ln), ref, REL_BF16 + 2.0 ** -8, pool=P, tail=True, rows=rows)
+    # pooled keys may differ by one BF16 ulp between the two sides (FP32 against
+    # float64 softmax pooling); the stated tolerance, relative to M, absorbs it
+    compare_topk(host(idx), host(sc), host(ln), ref, REL_BF16, pool=P, tail=True, rows=rows)
 
 
 def test_kpool_mxfp8_scoring():
@@ -63,7 +64,7 @@ def test_kpool_mxfp8_scoring():
     (dsa_idx_quantize_mxfp8) and scored against MXFP8 queries in pool mode.
     The oracle quantises its own pooled keys the same way; the two sides'
     pooled keys may differ by one BF16 ulp, which can move a key element by
-    one E4M3 step, hence the slack on top of the MXFP8 tolerance."""
+    one E4M3 step: the stated tolerance, relative to M, absorbs it."""
     wl = W.Workload("kpool-mx", [2600, 700], 64, 128, 2048, "mxfp8", "normal", w_std=0.125, kpool=4, seed=1007)
     x = W.make_inputs(wl)
     T, H, D, P = wl.total_tokens, wl.n_heads, wl.head_dim, wl.kpool
@@ -79,4 +80,4 @@ def test_kpool_mxfp8_scoring():
     rows = np.concatenate([np.arange(0, 40), np.arange(2560, 2620), np.arange(T - 40, T)])
     ref = O.kpool_topk(qq.reshape(T, H, D), kq, x["w"].astype(np.float64), wl.cu_seqlens, rcp, wl.index_topk, P,
                        True, rows=rows, with_scale=True)
-    compare_topk(host(idx), host(sc), host(ln), ref, REL_MXFP8 + 2.0 ** -6, pool=P, tail=True, rows=rows)
+    compare_topk(host(idx), host(sc), host(ln), ref, REL_MXFP8, pool=P, tail=True, rows=rows)

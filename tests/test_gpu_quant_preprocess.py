@@ -230,3 +230,36 @@ def test_preprocess_fp8_out(case):
     assert np.all(np.abs(gq - rq) <= step + 1e-30)
     stepk = np.ldexp(1.0, np.maximum(gks, rks).astype(int) - 127 + 8 - 3)[:, None]
     assert np.all(np.abs(gk - rk) <= stepk + 1e-30)
+
+
+@pytest.mark.parametrize("out_prec", ["mxfp8", "fp8", "bf16"])
+def test_fused_quantiser_bit_exact_on_its_input(out_prec):
+    """The fused preprocess with no key LayerNorm and no rotary dims on FP32
+    input: its carrier is the input itself, so the quantiser inside the fused
+    kernel must give the oracle's quantisation of that input bit for bit
+    (codes and scale bytes; BF16: the RNE bit patterns), queries and keys,
+    including the edge rows of the stand-alone quantiser test."""
+    rng = np.random.default_rng(17)
+    lens, H, D = [37, 5, 90], 8, 128
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    edge = _edge_rows(rng)
+    q = (rng.standard_normal((T * H, D)) * np.exp2(rng.integers(-20, 20, (T * H, 1)))).astype(np.float32)
+    q[:len(edge)] = edge
+    k = (rng.standard_normal((T, D)) * np.exp2(rng.integers(-20, 20, (T, 1)))).astype(np.float32)
+    k[:len(edge)] = edge[::-1]
+    q_op, q_sc, k_op, k_sc = dsa.preprocess(dev(q.reshape(T, H, D)), dev(k), dev(cu), max(lens), None, None,
+                                            1e-6, 0, 10000.0, False, True, out_prec)
+    if out_prec == "bf16":
+        np.testing.assert_array_equal(host(q_op.view(torch.int16)).view(np.uint16),
+                                      O.float_to_bf16_bits(O.round_bf16(q.astype(np.float64))))
+        np.testing.assert_array_equal(host(k_op.view(torch.int16)).view(np.uint16),
+                                      O.float_to_bf16_bits(O.round_bf16(k.astype(np.float64))))
+        return
+    quant = O.quantize_mxfp8 if out_prec == "mxfp8" else O.quantize_fp8_rows
+    rqc, rqs, _ = quant(q.astype(np.float64))
+    rkc, rks, _ = quant(k.astype(np.float64))
+    np.testing.assert_array_equal(host(q_sc).reshape(rqs.shape), rqs)
+    np.testing.assert_array_equal(host(q_op), rqc)
+    np.testing.assert_array_equal(host(k_sc).reshape(rks.shape), rks)
+    np.testing.assert_array_equal(host(k_op), rkc)

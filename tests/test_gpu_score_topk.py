@@ -206,8 +206,9 @@ def test_end_to_end_c2_like():
     rows = np.arange(0, T, 3)
     ref = O.indexer_topk(O.round_bf16(qf), O.round_bf16(kf), x["w"].astype(np.float64), wl.cu_seqlens,
                          wl.index_topk, rows=rows, with_scale=True)
-    # preprocessing differs by FP32 rounding: allow one extra BF16 ulp in the tolerance
-    compare_topk(host(idx), host(sc), host(ln), ref, REL_BF16 + 2.0 ** -8, rows=rows)
+    # the preprocessing chains differ by FP32 rounding (float64 on the oracle
+    # side); the stated tolerance, relative to M, applies as it is
+    compare_topk(host(idx), host(sc), host(ln), ref, REL_BF16, rows=rows, n_heads=H)
 
 
 def test_deterministic_replay():
