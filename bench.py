@@ -52,6 +52,36 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def measure_fp8_peak(device):
+    """Dense FP8 tensor throughput of this GPU, measured here: cuBLAS through
+    torch._scaled_mm on E4M3 operands, 8192^3, best of 10 (CUDA events), in
+    TFLOP/s.  Returns (value, source); falls back to the nominal FP8/BF16
+    ratio times the BF16 figure when the call is not available."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        one = torch.tensor(1.0, device=device)
+        for _ in range(3):
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        return 2.0 * n ** 3 / best / 1e9, "measured in this run: torch._scaled_mm E4M3 8192^3, best of 10"
+    except Exception as exc:   # noqa: BLE001
+        peaks, kind = load_peaks()
+        return (peaks["bf16_tflops"] * FP8_OVER_BF16,
+                f"{kind} bf16 burst x {FP8_OVER_BF16} (nominal FP8/BF16; FP8 GEMM unavailable: {exc})")
+
+
 def reduce_max_over_ranks(value, device):
     """Max of a per-rank float over the process group: the slowest rank sets
     the job's time.  Works with any backend (nccl on the GPUs, gloo on CPU)."""
@@ -206,6 +236,7 @@ def run_table(args):
     print(f"| config | precision | score+top-k ms | queries/s | TFLOP/s | % of {peak_kind} peak | "
           f"oracle queries/s ({os.cpu_count()} cores, rows) |")
     print("|---|---|---:|---:|---:|---:|---:|")
+    fp8_peak, _ = measure_fp8_peak(devn)
     for name, prec in cases:
         wl = W.config(name)
         x = W.make_inputs(wl)
@@ -244,11 +275,67 @@ def run_table(args):
             raise RuntimeError(f"{name} {prec}: device status {dsa.read_status(ws)}")
         ms = statistics.median(ts)
         tf = wl.flops() / ms / 1e9
-        peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if prec in ("mxfp8", "fp8") else 1.0)
+        peak = fp8_peak if prec in ("mxfp8", "fp8") else peaks["bf16_tflops"]
         n_rows = min(T, args.ref_rows // 8 if T > 4096 else 64)
         orate, _ = oracle_rate(wl, x, prec, n_rows)
         print(f"| {describe(wl, prec)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
               f"{100 * tf / peak:.1f} | {orate:,.1f} ({n_rows}) |", flush=True)
+
+
+def _median_ms(fn, flush, stream, reps=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    ts = []
+    for r in range(reps):
+        flush.fill_(r & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def time_hbm_kernels(dsa, q, T, H, D, flush, stream, peaks):
+    """The stand-alone HBM-bound kernels, each timed alone (CUDA events,
+    median of 5 after 2 warm-ups, L2 flushed before each): the MXFP8 and
+    per-vector FP8 quantisers on the workload's FP32 query rows, and KPool
+    compression (P = 4) of a 2^20-token FP32 key set.  GB/s from the
+    algorithmic bytes (read once, written once)."""
+    import torch
+    dev = q.device
+    out = {}
+    x = q.view(T * H, D)
+    codes = torch.empty((T * H, D), dtype=torch.uint8, device=dev)
+    s_mx = torch.empty((T * H, D // 32), dtype=torch.uint8, device=dev)
+    s_row = torch.empty((T * H,), dtype=torch.uint8, device=dev)
+    lib = dsa._abi.load()
+    st = stream.cuda_stream
+
+    def mx():
+        lib.dsa_idx_quantize_mxfp8(x.data_ptr(), 0, T * H, D, 0, codes.data_ptr(), s_mx.data_ptr(), st)
+
+    def f8():
+        lib.dsa_idx_quantize_fp8_rows(x.data_ptr(), 0, T * H, D, 0, codes.data_ptr(), s_row.data_ptr(), st)
+
+    n = T * H * D
+    for name, fn, nbytes in (("quantize_mxfp8", mx, n * 4 + n + n // 32), ("quantize_fp8_rows", f8, n * 4 + n + T * H)):
+        ms = _median_ms(fn, flush, stream)
+        out[name] = {"rows": T * H, "ms": ms, "bytes": nbytes, "GB/s": nbytes / ms / 1e6,
+                     "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+    del codes, s_mx, s_row
+    Tk, P = 1 << 20, 4
+    kk = torch.randn((Tk, D), device=dev)
+    gate = torch.randn(Tk, device=dev).to(torch.bfloat16).view(torch.int16)
+    bias = torch.randn(P, device=dev)
+    cuk = torch.tensor([0, Tk], dtype=torch.int32, device=dev)
+    nbytes = Tk * D * 4 + Tk * 2 + P * 4 + (Tk // P) * D * 2 + 8
+    ms = _median_ms(lambda: dsa.kpool_compress(kk, gate, bias, cuk, P), flush, stream)
+    out["kpool_compress"] = {"tokens": Tk, "pool": P, "ms": ms, "bytes": nbytes, "GB/s": nbytes / ms / 1e6,
+                             "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+    return out
 
 
 def run_reference(args, wl):
@@ -338,6 +425,7 @@ def run_native(args, wl):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    time.sleep(0.5)    # nvidia-smi's start-up holds the driver for a moment: keep it out of the timed loop
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                      # L2 flush, outside the events
@@ -445,12 +533,14 @@ def run_native(args, wl):
                 "frac_of_bf16_peak": wl.flops() / bms / 1e9 / peaks["bf16_tflops"],
                 "peak_tflops": peaks["bf16_tflops"], "peak_kind": peak_kind}
 
+    hbm_kernels = None if args.no_hbm else time_hbm_kernels(dsa, q, T, H, D, flush, stream, peaks)
+
     if rank != 0:
         return
     flops = wl.flops()
     sc_avg = statistics.mean(sc_ms)
     achieved = flops / sc_avg / 1e9                      # TFLOP/s
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp8_peak, fp8_src = measure_fp8_peak(devn)
     pre_bytes = T * H * D * 4 + T * D * 4 + T * H * D + T * H * D // 32 + T * D + T * D // 32
     tr = traffic_record()
     value = job_rate(world, T, args.steps, total_ms)
@@ -471,12 +561,13 @@ def run_native(args, wl):
                        "frac_of_hbm": pre_bytes / statistics.mean(pre_ms) / 1e6 / peaks["hbm_gbs"]},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak,
-                     "peak_source": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} (nominal FP8/BF16)",
+                     "peak_source": fp8_src,
                      "kernel": "score_topk call (work list + key-scale layout + fused kernel; the fused "
                                "kernel is 99.7 % of it), events on the launch stream",
                      "traffic": tr["bytes_per_launch"] if tr else None,
                      "traffic_source": tr["scaled_to"] if tr else None},
         "bf16_scoring": bf16,
+        "hbm_kernels": hbm_kernels,
         "e2e": {"value": job_rate(world, T, 1, e2e_ms), "unit": "queries/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host q,k,w -> dsa_idx_preprocess -> dsa_idx_score_topk -> host top-k indices; "
@@ -485,7 +576,9 @@ def run_native(args, wl):
         # MXFP8 key-scale layout, fused kernel)
         "gpu_launches": (4 if prec == "mxfp8" else 3) * args.steps,
         "clocks": clk,
-        "wall_s": t_wall,
+        # host clock around the timed loop: the K steps plus the L2 flush before
+        # each one (a 256 MB write) and the launch overhead
+        "timed_loop_wall_s": t_wall,
         "cpu_baseline": None if cpu_rate is None else {
             "value": cpu_rate, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{args.ref_rows} query rows of the target at seeded uniform positions "
@@ -504,6 +597,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=3072)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-hbm", action="store_true", help="skip timing the stand-alone HBM-bound kernels")
     ap.add_argument("--table", action="store_true",
                     help="time every configuration and print a markdown table instead of the JSON line")
     args = ap.parse_args()

@@ -234,9 +234,10 @@ dsa_status_t dsa_idx_kpool_compress(
  *   ws, ws_bytes  device workspace of dsa_idx_workspace_size() bytes
  * Ties are broken towards the lower index; -0 and +0 compare equal.
  * Supported: head_dim 128 (BF16 also 64), n_heads in {4,8,16,32,64},
- * 1 <= index_topk <= 2048 (MXFP8 or FP8 with 4 heads: <= 1664, the candidate
- * buffers of its 12 queries per block must fit in shared memory),
- * max_seqlen <= 65536.  Other shapes return DSA_ERR_UNSUPPORTED. */
+ * 1 <= index_topk <= 4096 (KPool: at most 4096 pools, index_topk <= 4096 *
+ * kpool_size; MXFP8 or FP8 with 4 heads: <= 1664, the candidate buffers of
+ * its 12 queries per block must fit in shared memory), max_seqlen <= 65536.
+ * Other shapes return DSA_ERR_UNSUPPORTED. */
 dsa_status_t dsa_idx_score_topk(
     const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
     const void* w, dsa_dtype_t w_dtype, float sm_scale,
@@ -281,14 +282,20 @@ dsa_status_t dsa_idx_score_topk_kv(
  * Same arguments and results as dsa_idx_score_topk without ws/ws_bytes.  The
  * scratch lives in a fixed 4 MiB device array inside the library, which every
  * GPU that loads the library holds until the process exits; sizes whose
- * dsa_idx_workspace_size exceeds 4 MiB (roughly total_tokens + num_seqs above
- * 520000) are rejected with DSA_ERR_WORKSPACE before anything is launched.
- * It calls no cudaMalloc/cudaFree.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before capturing any stream.  All calls share the one
- * array, so calls whose GPU work overlaps (other streams, or unordered calls
- * from several host threads) race on it; the device status word of the last
- * call is not readable through this entry point. */
+ * dsa_idx_workspace_size exceeds 4 MiB are rejected with DSA_ERR_WORKSPACE
+ * before anything is launched: about total_tokens + num_seqs above 524 000 for
+ * BF16 and FP8 scoring, and total_tokens above about 349 000 for MXFP8 (its
+ * per-tile key scales also live in the scratch; each document costs about 43
+ * tokens' worth more).  Comparing dsa_idx_workspace_size with 4194304 gives
+ * the exact answer.  It calls no cudaMalloc/cudaFree.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current and keeps it once found (a failed lookup is retried by the
+ * next call); make that first call before capturing any stream.  The address
+ * is that of the current CUDA context: a device reset while the library is
+ * loaded is not supported.  All calls share the one array, so calls whose GPU
+ * work overlaps (other streams, or unordered calls from several host threads)
+ * race on it.  dsa_idx_score_topk_noalloc_status reads the device status word
+ * the last call left in the array. */
 dsa_status_t dsa_idx_score_topk_noalloc(
     const void* q, const uint8_t* q_scale, const void* k, const uint8_t* k_scale,
     const void* w, dsa_dtype_t w_dtype, float sm_scale,
@@ -296,6 +303,15 @@ dsa_status_t dsa_idx_score_topk_noalloc(
     int n_heads, int head_dim, int index_topk, dsa_precision_t prec, int flags,
     int kpool_size, const int32_t* cu_pools,
     int32_t* topk_idx, float* topk_score, int32_t* topk_len, dsa_stream_t stream);
+
+/* Companion of dsa_idx_score_topk_noalloc (no counterpart in the pages):
+ * synchronise `stream` and return in *out the device status word the last
+ * dsa_idx_score_topk_noalloc call on the current device left in the library's
+ * scratch array: DSA_ERR_TIMEOUT when a bounded device wait ran out (the
+ * rows of that call are then incomplete), DSA_ERR_INVALID_ARG when the device
+ * found cu_seqlens inconsistent, DSA_OK otherwise.  Eager helper, like
+ * dsa_idx_read_status; do not call it while capturing a graph. */
+dsa_status_t dsa_idx_score_topk_noalloc_status(dsa_stream_t stream, dsa_status_t* out);
 
 /* Synchronise `stream` and return the device status word recorded in `ws` by
  * the last dsa_idx_score_topk call on it (DSA_OK if none).  Eager helper; do

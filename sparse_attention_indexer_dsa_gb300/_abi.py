@@ -58,6 +58,7 @@ SIGNATURES = {
     "dsa_idx_score_topk_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                             _vp, _vp, _vp, _vp]),
+    "dsa_idx_score_topk_noalloc_status": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
     "dsa_idx_read_status": (_c_int, [_vp, _vp, ctypes.POINTER(_c_int)]),
     "dsa_idx_debug_mma_tile": (_c_int, [_vp, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i64, _c_int,
                                         _c_int, _c_int, _vp, _vp, _c_size, _vp]),

@@ -339,8 +339,8 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
     if (index_topk % kpool_size != 0) return fail(DSA_ERR_INVALID_ARG, "index_topk must be a multiple of kpool_size");
   }
   const int expand = kpool_size > 1 && !compressed ? kpool_size : 1;   // tokens per selected key in the output
-  if (index_topk < 1 || index_topk > 2048 * expand)
-    return fail(DSA_ERR_UNSUPPORTED, "index_topk must be in [1, 2048] (pools)");
+  if (index_topk < 1 || index_topk > kMaxKeep * expand)
+    return fail(DSA_ERR_UNSUPPORTED, "index_topk must be in [1, 4096] (KPool: at most 4096 pools)");
   const int keep = index_topk / expand;
   if (keep < 1) return fail(DSA_ERR_INVALID_ARG, "index_topk / kpool_size must be >= 1");
   if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
@@ -413,7 +413,7 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   e = launch_score_topk(p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "score_topk launch");
   if (rank_order) {
-    e = launch_rank_rows(topk_idx, topk_score, total_tokens, p.out_width, di.sm_count, st);
+    e = launch_rank_rows(topk_idx, topk_score, total_tokens, p.out_width, expand, di.sm_count, st);
     if (e != cudaSuccess) return cuda_fail(e, "rank_rows launch");
   }
   return DSA_OK;

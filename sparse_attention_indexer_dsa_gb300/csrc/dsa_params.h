@@ -52,8 +52,9 @@ cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const i
                                  int sm_count, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_debug_mma_tile(const DebugParams& p, int prec, cudaStream_t stream);
-// Reorders each finished top-k row into ranking order (score desc, index asc).
-cudaError_t launch_rank_rows(int32_t* idx, float* score, int64_t rows, int width, int sm_count,
+// Reorders each finished top-k row into ranking order (score desc, index asc),
+// moving units of `group` consecutive entries (1, or the KPool pool size).
+cudaError_t launch_rank_rows(int32_t* idx, float* score, int64_t rows, int width, int group, int sm_count,
                              cudaStream_t stream);
 
 }  // namespace dsa

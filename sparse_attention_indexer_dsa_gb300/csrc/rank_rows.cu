@@ -2,17 +2,20 @@
 // descending, index ascending, the order of the repeated-varlen-ends rows in
 // PR #8403's review ("Preservation and acceptance").  A pass over the rows
 // the fused kernel wrote, so the fused kernel itself is the same in either
-// order.  One CTA of 128 threads per row (grid-stride).  The row's rankable
+// order.  One CTA of 256 threads per row (grid-stride).  The row's rankable
 // prefix (valid entries with a finite score; KPool tail tokens, scored +INF,
 // stay last) arrives in ascending index order, so a stable sort on the
 // order-preserving 32-bit score key alone gives the ranking: a block radix
-// sort, least significant 4-bit digit first, E entries a thread, skipping
-// the digits on which every entry agrees.  Per digit: each thread counts its
-// entries in its own column of a digit-major counter table, one block scan
-// turns the counts into destinations, and the entries are scattered through
-// shared memory (slot index padded by one per 32, conflict-free).  Indices
-// are below 65536 in every mode, and the fused kernel writes canonical scores
-// (-0 as +0), so the round trip through the key is exact.
+// sort, least significant 4-bit digit first, E units a thread, skipping the
+// digits on which every unit agrees.  In KPool mode the unit is a pool (its
+// P consecutive tokens share one score and move together), so rows of up to
+// 4096 pools rank at pool granularity.  Per digit: each thread counts its
+// units in its own column of a digit-major counter table, one block scan
+// turns the counts into destinations, and the units
+// are scattered through shared memory (slot index padded by one per 32,
+// conflict-free).  Indices are below 65536 in every mode, and the fused
+// kernel writes canonical scores (-0 as +0), so the round trip through the
+// key is exact.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,8 +24,9 @@
 namespace dsa {
 namespace {
 
-constexpr int kRankThreads = 128;
-constexpr int kRankMaxSlots = 2048;   // index_topk <= 2048 entries carry a finite score
+constexpr int kRankThreads = 256;
+constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kRankMaxUnits = 4096;   // index_topk <= 4096 (KPool: pools) carry a finite score
 constexpr int kDigits = 16;           // 4-bit digits
 
 __device__ __forceinline__ int padded(int g) { return g + (g >> 5); }
@@ -38,20 +42,20 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 }
 
 struct RankSmem {
-  uint32_t key[kRankMaxSlots + kRankMaxSlots / 32];
-  uint16_t idx[kRankMaxSlots + kRankMaxSlots / 32];
+  uint32_t key[kRankMaxUnits + kRankMaxUnits / 32];
+  uint16_t idx[kRankMaxUnits + kRankMaxUnits / 32];
   uint32_t cnt[kDigits * kRankThreads + kDigits * kRankThreads / 32];   // digit-major, padded
-  uint32_t red[8];
+  uint32_t red[2 * kRankWarps];
   int n;
 };
 
-// Sorts entries 0 .. n-1 of sm (padded slots; entries n .. 128E-1 hold key 0,
-// index 0xFFFF) by key descending, stably.  Thread t holds entries tE .. tE+E-1.
+// Sorts units 0 .. n-1 of sm (padded slots; units n .. 256E-1 hold key 0,
+// index 0xFFFF) by key descending, stably.  Thread t holds units tE .. tE+E-1.
 template <int E>
 __device__ __forceinline__ void rank_sort(RankSmem& sm, int n, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t key[E], idx[E];
-  uint32_t vor = 0u, vand = 0xFFFFFFFFu;   // over the real entries only
+  uint32_t vor = 0u, vand = 0xFFFFFFFFu;   // over the real units only
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int g = tid * E + e;
@@ -66,16 +70,21 @@ __device__ __forceinline__ void rank_sort(RankSmem& sm, int n, int tid) {
   vand = __reduce_and_sync(0xffffffffu, vand);
   if (lane == 0) {
     sm.red[warp] = vor;
-    sm.red[4 + warp] = vand;
+    sm.red[kRankWarps + warp] = vand;
   }
   __syncthreads();
-  const uint32_t vary = (sm.red[0] | sm.red[1] | sm.red[2] | sm.red[3]) ^
-                        (sm.red[4] & sm.red[5] & sm.red[6] & sm.red[7]);
+  uint32_t all_or = 0u, all_and = 0xFFFFFFFFu;
+#pragma unroll
+  for (int w = 0; w < kRankWarps; ++w) {
+    all_or |= sm.red[w];
+    all_and &= sm.red[kRankWarps + w];
+  }
+  const uint32_t vary = all_or ^ all_and;
   __syncthreads();   // red is reused by the scans
 #pragma unroll 1
   for (int shift = 0; shift < 32; shift += 4) {
-    if (((vary >> shift) & 0xFu) == 0u) continue;   // every entry has the same digit: order kept
-    // 1. count: digit' = 15 - digit (descending keys), rank among this thread's earlier entries
+    if (((vary >> shift) & 0xFu) == 0u) continue;   // every unit has the same digit: order kept
+    // 1. count: digit' = 15 - digit (descending keys), rank among this thread's earlier units
 #pragma unroll
     for (int d = 0; d < kDigits; ++d) sm.cnt[padded(d * kRankThreads + tid)] = 0u;
     uint32_t dg[E], rk[E];
@@ -128,55 +137,87 @@ __device__ __forceinline__ void rank_sort(RankSmem& sm, int n, int tid) {
   }
 }
 
+// One row per CTA iteration.  A unit is `group` consecutive entries with one
+// score: a single entry (group 1), or one KPool pool whose tokens are
+// consecutive (group = pool size); units move as a whole, so a pool's tokens
+// stay together and ascending.
+template <int E>
 __global__ void __launch_bounds__(kRankThreads) rank_rows_kernel(int32_t* idx, float* score, int64_t rows,
-                                                                  int width) {
+                                                                  int width, int group) {
   __shared__ RankSmem sm;
   const int tid = threadIdx.x;
+  const int nu_max = min((width + group - 1) / group, kRankMaxUnits);
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     int32_t* ri = idx + r * width;
     float* rs = score + r * width;
     if (tid == 0) sm.n = 0;
     __syncthreads();
-    // the rankable entries are a prefix of the row: valid (index >= 0) with a finite score
+    // the rankable units are a prefix of the row: valid (index >= 0) with a finite score;
+    // every load of the row is issued before any is used
+    int32_t li[E];
+    float ls[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int u = e * kRankThreads + tid;
+      li[e] = u < nu_max ? ri[(size_t)u * group] : -1;
+      ls[e] = u < nu_max ? rs[(size_t)u * group] : 0.f;
+    }
     int last = 0;
-    for (int g = tid; g < width; g += kRankThreads)
-      if (ri[g] >= 0 && rs[g] != __int_as_float(0x7f800000)) last = g + 1;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int u = e * kRankThreads + tid;
+      if (li[e] >= 0 && ls[e] != __int_as_float(0x7f800000)) last = u + 1;
+    }
     if (last > 0) atomicMax(&sm.n, last);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int g = e * kRankThreads + tid;
+      sm.key[padded(g)] = li[e] >= 0 ? score_key(ls[e]) : 0u;
+      sm.idx[padded(g)] = li[e] >= 0 ? (uint16_t)li[e] : (uint16_t)0xFFFFu;
+    }
     __syncthreads();
-    const int n = sm.n < kRankMaxSlots ? sm.n : kRankMaxSlots;
+    const int n = sm.n;
     if (n > 1) {
-      int np = kRankThreads;
-      while (np < n) np <<= 1;
-      for (int g = tid; g < np; g += kRankThreads) {
-        sm.key[padded(g)] = g < n ? score_key(rs[g]) : 0u;
-        sm.idx[padded(g)] = g < n ? (uint16_t)ri[g] : (uint16_t)0xFFFFu;
+      // units n .. 256E-1 (padding, +INF tail) sort after every real unit
+      for (int g = n + tid; g < E * kRankThreads; g += kRankThreads) {
+        sm.key[padded(g)] = 0u;
+        sm.idx[padded(g)] = (uint16_t)0xFFFFu;
       }
       __syncthreads();
-      switch (np / kRankThreads) {
-        case 1: rank_sort<1>(sm, n, tid); break;
-        case 2: rank_sort<2>(sm, n, tid); break;
-        case 4: rank_sort<4>(sm, n, tid); break;
-        case 8: rank_sort<8>(sm, n, tid); break;
-        default: rank_sort<16>(sm, n, tid); break;
-      }
-      for (int g = tid; g < n; g += kRankThreads) {
-        ri[g] = (int32_t)sm.idx[padded(g)];
-        rs[g] = key_score(sm.key[padded(g)]);
+      rank_sort<E>(sm, n, tid);
+      for (int g = tid; g < n * group; g += kRankThreads) {
+        const int u = g / group;
+        ri[g] = (int32_t)sm.idx[padded(u)] + (g - u * group);
+        rs[g] = key_score(sm.key[padded(u)]);
       }
     }
     __syncthreads();   // n and the slots are reused by the next row
   }
 }
 
-}  // namespace
-
-cudaError_t launch_rank_rows(int32_t* idx, float* score, int64_t rows, int width, int sm_count,
-                             cudaStream_t stream) {
-  if (rows <= 0) return cudaSuccess;
+template <int E>
+cudaError_t launch_e(int32_t* idx, float* score, int64_t rows, int width, int group, int sm_count,
+                     cudaStream_t stream) {
   int64_t grid = (int64_t)sm_count * 8;
   if (grid > rows) grid = rows;
-  rank_rows_kernel<<<(unsigned)grid, kRankThreads, 0, stream>>>(idx, score, rows, width);
+  rank_rows_kernel<E><<<(unsigned)grid, kRankThreads, 0, stream>>>(idx, score, rows, width, group);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rank_rows(int32_t* idx, float* score, int64_t rows, int width, int group, int sm_count,
+                             cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  // at most kRankMaxUnits units are rankable (the API keeps at most 4096 keys or
+  // pools per row); a KPool tail beyond them is never ranked and stays in place
+  int units = (width + group - 1) / group;
+  if (units > kRankMaxUnits) units = kRankMaxUnits;
+  if (units <= 1 * kRankThreads) return launch_e<1>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 2 * kRankThreads) return launch_e<2>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 4 * kRankThreads) return launch_e<4>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 8 * kRankThreads) return launch_e<8>(idx, score, rows, width, group, sm_count, stream);
+  return launch_e<16>(idx, score, rows, width, group, sm_count, stream);
 }
 
 }  // namespace dsa

@@ -23,6 +23,7 @@ constexpr int kMaxQpw = 4;           // queries per epilogue warpgroup (at most)
 constexpr int kMiscInts = 192 + 2 * kBatch * kMaxQpw * 4;   // per-warpgroup scratch ints
 constexpr int kMaxStages = 6;
 constexpr int kMaxCand = 8192;      // candidate entries per query (at most)
+constexpr int kMaxKeep = 4096;      // entries (KPool: pools) kept per query (at most)
 constexpr int kSfaCol = 384;         // MXFP8: key scales, 2 x 4 TMEM columns (alternating per tile)
 constexpr int kSfbCol = 392;         // MXFP8: query scales, up to 2 atoms x 4 columns
 

@@ -62,10 +62,16 @@ def test_host_argument_checks_precede_any_cuda_call(lib):
     rc = lib.dsa_idx_score_topk(P(256), None, P(256), None, P(256), 0, 1.0, P(256), 1, 16, 16, 64, 128,
                                 16, 0, 1, 1, None, P(256), None, None, P(256), 16, None)
     assert rc == _abi.DSA_ERR_WORKSPACE
-    # top-k beyond the on-chip limit
+    # top-k beyond the supported 4096
     rc = lib.dsa_idx_score_topk(P(256), None, P(256), None, P(256), 0, 1.0, P(256), 1, 16, 16, 64, 128,
-                                4096, 0, 1, 1, None, P(256), None, None, P(256), 1 << 20, None)
+                                4097, 0, 1, 1, None, P(256), None, None, P(256), 1 << 20, None)
     assert rc == _abi.DSA_ERR_UNSUPPORTED
+    # KPool: at most 4096 pools
+    rc = lib.dsa_idx_score_topk(P(256), None, P(256), None, P(256), 0, 1.0, P(256), 1, 16, 16, 64, 128,
+                                4 * 4097, 0, 1, 4, P(256), P(256), None, None, P(256), 1 << 20, None)
+    assert rc == _abi.DSA_ERR_UNSUPPORTED
+    # the no-allocation status reader needs somewhere to put the status
+    assert lib.dsa_idx_score_topk_noalloc_status(None, None) == _abi.DSA_ERR_INVALID_ARG
     # misaligned tensor
     rc = lib.dsa_idx_quantize_mxfp8(P(257), 0, 4, 128, 0, P(256), P(256), None)
     assert rc == _abi.DSA_ERR_INVALID_ARG
@@ -124,7 +130,7 @@ def test_score_plan_fits_every_supported_shape(lib):
     P = ctypes.c_void_p
     for prec, D in ((0, 128), (0, 64), (1, 128), (2, 128)):
         for H in (4, 8, 16, 32, 64):
-            for k in ((1, 32, 256, 1024) if (prec != 0 and H == 4) else (1, 32, 256, 2048)):
+            for k in ((1, 32, 256, 1024) if (prec != 0 and H == 4) else (1, 32, 256, 2048, 3000, 4096)):
                 rc = lib.dsa_idx_score_topk(P(256), P(256), P(256), P(256), P(256), 0, 1.0, P(256), 1, 0, 0,
                                             H, D, k, prec, 1, 1, None, P(256), None, None, P(256), 1 << 20, None)
                 assert rc in (_abi.DSA_OK, _abi.DSA_ERR_CUDA, _abi.DSA_ERR_UNSUPPORTED), (prec, D, H, k, rc)
