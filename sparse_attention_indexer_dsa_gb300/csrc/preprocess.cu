@@ -109,11 +109,12 @@ __device__ __forceinline__ void load_row(const void* base, int in_bf16, size_t r
 }
 
 constexpr int kPreThreads = 256;
+constexpr int kPreMinBlocks = 4;   // resident blocks per SM: 64 registers a thread, no spills
 constexpr int kPreMaxRows = 9;   // ceil((64 query heads + 1 key) / 8 warps)
 
 // One block per token.  Row r < H is query head r, row H is the key.
 template <int D>
-__global__ void __launch_bounds__(kPreThreads) preprocess_kernel(const __grid_constant__ PreParams p) {
+__global__ void __launch_bounds__(kPreThreads, kPreMinBlocks) preprocess_kernel(const __grid_constant__ PreParams p) {
   constexpr int VEC = D / 32;
   __shared__ float s_cos[64], s_sin[64];
   __shared__ int s_pos;

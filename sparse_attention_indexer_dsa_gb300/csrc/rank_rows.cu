@@ -2,7 +2,8 @@
 // descending, index ascending, the order of the repeated-varlen-ends rows in
 // PR #8403's review ("Preservation and acceptance").  A pass over the rows
 // the fused kernel wrote, so the fused kernel itself is the same in either
-// order.  One CTA of 256 threads per row (grid-stride).  The row's rankable
+// order.  One CTA of 128 threads per row of up to 2048 units, 256 threads up
+// to 4096 (grid-stride).  The row's rankable
 // prefix (valid entries with a finite score; KPool tail tokens, scored +INF,
 // stay last) arrives in ascending index order, so a stable sort on the
 // order-preserving 32-bit score key alone gives the ranking: a block radix
@@ -24,8 +25,6 @@
 namespace dsa {
 namespace {
 
-constexpr int kRankThreads = 256;
-constexpr int kRankWarps = kRankThreads / 32;
 constexpr int kRankMaxUnits = 4096;   // index_topk <= 4096 (KPool: pools) carry a finite score
 constexpr int kDigits = 16;           // 4-bit digits
 
@@ -41,18 +40,23 @@ __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// NT threads rank up to 16 * NT units (128 threads up to 2048, 256 up to 4096:
+// the smaller block keeps more rows in flight per SM).
+template <int NT>
 struct RankSmem {
-  uint32_t key[kRankMaxUnits + kRankMaxUnits / 32];
-  uint16_t idx[kRankMaxUnits + kRankMaxUnits / 32];
-  uint32_t cnt[kDigits * kRankThreads + kDigits * kRankThreads / 32];   // digit-major, padded
-  uint32_t red[2 * kRankWarps];
+  static constexpr int kUnits = 16 * NT;
+  uint32_t key[kUnits + kUnits / 32];
+  uint16_t idx[kUnits + kUnits / 32];
+  uint32_t cnt[kDigits * NT + kDigits * NT / 32];   // digit-major, padded
+  uint32_t red[2 * (NT / 32)];
   int n;
 };
 
 // Sorts units 0 .. n-1 of sm (padded slots; units n .. 256E-1 hold key 0,
 // index 0xFFFF) by key descending, stably.  Thread t holds units tE .. tE+E-1.
-template <int E>
-__device__ __forceinline__ void rank_sort(RankSmem& sm, int n, int tid) {
+template <int NT, int E>
+__device__ __forceinline__ void rank_sort(RankSmem<NT>& sm, int n, int tid) {
+  constexpr int kRankThreads = NT, kRankWarps = NT / 32;
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t key[E], idx[E];
   uint32_t vor = 0u, vand = 0xFFFFFFFFu;   // over the real units only
@@ -141,12 +145,13 @@ __device__ __forceinline__ void rank_sort(RankSmem& sm, int n, int tid) {
 // score: a single entry (group 1), or one KPool pool whose tokens are
 // consecutive (group = pool size); units move as a whole, so a pool's tokens
 // stay together and ascending.
-template <int E>
-__global__ void __launch_bounds__(kRankThreads) rank_rows_kernel(int32_t* idx, float* score, int64_t rows,
-                                                                  int width, int group) {
-  __shared__ RankSmem sm;
+template <int NT, int E>
+__global__ void __launch_bounds__(NT) rank_rows_kernel(int32_t* idx, float* score, int64_t rows, int width,
+                                                       int group) {
+  constexpr int kRankThreads = NT;
+  __shared__ RankSmem<NT> sm;
   const int tid = threadIdx.x;
-  const int nu_max = min((width + group - 1) / group, kRankMaxUnits);
+  const int nu_max = min((width + group - 1) / group, RankSmem<NT>::kUnits);
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     int32_t* ri = idx + r * width;
     float* rs = score + r * width;
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kRankThreads) rank_rows_kernel(int32_t* idx, f
         sm.idx[padded(g)] = (uint16_t)0xFFFFu;
       }
       __syncthreads();
-      rank_sort<E>(sm, n, tid);
+      rank_sort<NT, E>(sm, n, tid);
       for (int g = tid; g < n * group; g += kRankThreads) {
         const int u = g / group;
         ri[g] = (int32_t)sm.idx[padded(u)] + (g - u * group);
@@ -195,12 +200,12 @@ __global__ void __launch_bounds__(kRankThreads) rank_rows_kernel(int32_t* idx, f
   }
 }
 
-template <int E>
+template <int NT, int E>
 cudaError_t launch_e(int32_t* idx, float* score, int64_t rows, int width, int group, int sm_count,
                      cudaStream_t stream) {
   int64_t grid = (int64_t)sm_count * 8;
   if (grid > rows) grid = rows;
-  rank_rows_kernel<E><<<(unsigned)grid, kRankThreads, 0, stream>>>(idx, score, rows, width, group);
+  rank_rows_kernel<NT, E><<<(unsigned)grid, NT, 0, stream>>>(idx, score, rows, width, group);
   return cudaGetLastError();
 }
 
@@ -213,11 +218,12 @@ cudaError_t launch_rank_rows(int32_t* idx, float* score, int64_t rows, int width
   // pools per row); a KPool tail beyond them is never ranked and stays in place
   int units = (width + group - 1) / group;
   if (units > kRankMaxUnits) units = kRankMaxUnits;
-  if (units <= 1 * kRankThreads) return launch_e<1>(idx, score, rows, width, group, sm_count, stream);
-  if (units <= 2 * kRankThreads) return launch_e<2>(idx, score, rows, width, group, sm_count, stream);
-  if (units <= 4 * kRankThreads) return launch_e<4>(idx, score, rows, width, group, sm_count, stream);
-  if (units <= 8 * kRankThreads) return launch_e<8>(idx, score, rows, width, group, sm_count, stream);
-  return launch_e<16>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 128) return launch_e<128, 1>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 256) return launch_e<128, 2>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 512) return launch_e<128, 4>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 1024) return launch_e<128, 8>(idx, score, rows, width, group, sm_count, stream);
+  if (units <= 2048) return launch_e<128, 16>(idx, score, rows, width, group, sm_count, stream);
+  return launch_e<256, 16>(idx, score, rows, width, group, sm_count, stream);
 }
 
 }  // namespace dsa
