@@ -753,71 +753,64 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     // One MMA chain per key tile covering every query of the item (N = ncols),
-    // into TMEM slot tcount & 1 (double buffered).
-    PT_DECL
-    uint32_t tcount = 0, st = 0, ph = 0;
-    int it = 0;
-    bool ok = true;
-    const uint32_t idesc = MX ? 0u : (F8 ? idesc_f8(128, pl.ncols) : idesc_bf16(128, pl.ncols));
-    uint32_t idesc_k[4];
+    // into TMEM slot tcount & 1 (double buffered).  Lane 0 alone runs the loop:
+    // the fewest instructions between a freed slot and the issued MMAs (this
+    // warp shares its SM sub-partition with three busy epilogue warps).
+    if (lane == 0) {
+      PT_DECL
+      uint32_t tcount = 0, st = 0, ph = 0;
+      int it = 0;
+      bool ok = true;
+      const uint32_t idesc = MX ? 0u : (F8 ? idesc_f8(128, pl.ncols) : idesc_bf16(128, pl.ncols));
+      uint32_t idesc_k[4];
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) idesc_k[kk] = idesc_mxf8(128, pl.ncols, kk);
-    const uint64_t a_desc0 = sw128_kmajor_desc(sbase + pl.k_off, 0);    // stage 0, K step 0
-    const uint64_t b_desc0 = sw128_kmajor_desc(sbase + pl.q_off, 0);    // chunk 0, K step 0
-    const uint64_t sf_desc0 = sf_src_desc(sbase + pl.sfa_tx_off);       // stage 0 key scales
-    for (int r = 0; ok && r * G < nitems; ++r) {
-      const int i = item_index(r, nitems);
-      if (i < 0) continue;
-      const Item m = load_item(p, i);
-      if (m.ntiles == 0) continue;
-      PT_MARK();
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_qfull, it & 1, abort_flag, status, tmo))) {
-        ok = false;
-        break;
-      }
-      PT_ADD(0);
-      if (MX) {
-        for (int a = 0; a < pl.sfb_atoms; ++a)
-          transpose_scales(reinterpret_cast<const uint32_t*>(smem + pl.sfb_raw_off + a * kSfRawBytes),
-                           0, reinterpret_cast<uint32_t*>(smem + pl.sfb_tx_off + a * kSfTxBytes),
-                           lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tc_fence_after();
-          for (int a = 0; a < pl.sfb_atoms; ++a)
-            tc_cp_32x128b_warpx4(tmem + kSfbCol + 4 * a,
-                                 sf_src_desc(sbase + pl.sfb_tx_off + a * kSfTxBytes));
-        }
-        __syncwarp();
-      }
-      for (int t = 0; ok && t < m.ntiles; ++t) {
-        const uint32_t slot = tcount & 1;
+      for (int kk = 0; kk < 4; ++kk) idesc_k[kk] = idesc_mxf8(128, pl.ncols, kk);
+      const uint64_t a_desc0 = sw128_kmajor_desc(sbase + pl.k_off, 0);    // stage 0, K step 0
+      const uint64_t b_desc0 = sw128_kmajor_desc(sbase + pl.q_off, 0);    // chunk 0, K step 0
+      const uint64_t sf_desc0 = sf_src_desc(sbase + pl.sfa_tx_off);       // stage 0 key scales
+      for (int r = 0; ok && r * G < nitems; ++r) {
+        const int i = item_index(r, nitems);
+        if (i < 0) continue;
+        const Item m = load_item(p, i);
+        if (m.ntiles == 0) continue;
         PT_MARK();
-        const bool got = tcount < 2 ||
-                         mbar_wait(bar_tempty(slot), ((tcount >> 1) - 1) & 1, abort_flag, status, tmo);
-        if (!__all_sync(0xffffffffu, got)) {
+        if (!mbar_wait(bar_qfull, it & 1, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
-        PT_ADD(1);
-        TRACE(0, tcount, lane == 0);   // the tile's TMEM slot is free
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + slot * pl.ncols;
-        for (int c = 0; c < pl.chunks; ++c) {
+        PT_ADD(0);
+        if (MX) {   // query scales of the item, re-laid out for tcgen05.cp
+          for (int a = 0; a < pl.sfb_atoms; ++a) {
+            const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + pl.sfb_raw_off + a * kSfRawBytes);
+            uint4* tx = reinterpret_cast<uint4*>(smem + pl.sfb_tx_off + a * kSfTxBytes);
+            for (int l = 0; l < 32; ++l) tx[l] = make_uint4(raw[l], raw[l + 32], raw[l + 64], raw[l + 96]);
+          }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          for (int a = 0; a < pl.sfb_atoms; ++a)
+            tc_cp_32x128b_warpx4(tmem + kSfbCol + 4 * a, sf_src_desc(sbase + pl.sfb_tx_off + a * kSfTxBytes));
+        }
+        for (int t = 0; t < m.ntiles; ++t) {
+          const uint32_t slot = tcount & 1;
           PT_MARK();
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), ph, abort_flag, status, tmo))) {
+          if (tcount >= 2 && !mbar_wait(bar_tempty(slot), ((tcount >> 1) - 1) & 1, abort_flag, status, tmo)) {
             ok = false;
             break;
           }
-          PT_ADD(2);
-          TRACE(14, tcount, lane == 0 && c == 0);   // the tile's K stage has landed
-          if (lane == 0) {
+          PT_ADD(1);
+          TRACE(0, tcount, true);   // the tile's TMEM slot is free
+          const uint32_t d_tmem = tmem + slot * pl.ncols;
+          const uint32_t sfa = tmem + kSfaCol + 4 * (tcount & 1);   // alternates per tile
+          for (int c = 0; c < pl.chunks; ++c) {
+            if (!mbar_wait(bar_full(st), ph, abort_flag, status, tmo)) {
+              ok = false;
+              break;
+            }
+            TRACE(14, tcount, c == 0);   // the tile's K stage has landed
             tc_fence_after();
             // descriptors: start address field + 2 per 32-byte K step
             const uint64_t ad0 = a_desc0 + (uint64_t)(st * (kStageBytes >> 4));
             const uint64_t bd0 = b_desc0 + (uint64_t)(c * (pl.qchunk >> 4));
-            const uint32_t sfa = tmem + kSfaCol + 4 * (tcount & 1);   // alternates per tile
             if (MX)   // key scales arrive laid out for tcgen05.cp with the stage
               tc_cp_32x128b_warpx4(sfa, sf_desc0 + (uint64_t)(st * (kSfTxBytes >> 4)));
 #pragma unroll
@@ -831,30 +824,25 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
                 mma_bf16(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
             }
             tc_commit(bar_empty(st));
+            if (++st == (uint32_t)nst) {
+              st = 0;
+              ph ^= 1u;
+            }
           }
-          __syncwarp();
+          if (!ok) break;
           PT_ADD(3);
-          if (++st == (uint32_t)nst) {
-            st = 0;
-            ph ^= 1u;
-          }
+          TRACE(1, tcount, true);   // MMAs of the tile issued
+          tc_commit(bar_tfull(slot));
+          ++tcount;
         }
         if (!ok) break;
-        TRACE(1, tcount, lane == 0);   // MMAs of the tile issued
-        if (lane == 0) tc_commit(bar_tfull(slot));
-        __syncwarp();
-        ++tcount;
+        tc_commit(bar_qempty);
+        ++it;
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(bar_qempty);
-      __syncwarp();
-      ++it;
-    }
-    if (lane == 0) {
       tc_commit(bar_drain);
       drain_wait(bar_drain, 0, tmo);
+      PT_FLUSH(8, true);
     }
-    PT_FLUSH(8, lane == 0);
     __syncwarp();
   } else {
     // ======================= epilogue warpgroups =======================
