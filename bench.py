@@ -338,6 +338,36 @@ def time_hbm_kernels(dsa, q, T, H, D, flush, stream, peaks):
     return out
 
 
+def run_hbm_only(args, wl):
+    """The HBM-bound kernels alone on the workload's inputs (preprocess in
+    the workload's precision, the stand-alone quantisers, KPool compression):
+    one JSON line of GB/s figures.  Used for their ncu captures."""
+    import torch
+    import sparse_attention_indexer_dsa_gb300 as dsa
+
+    torch.cuda.set_device(0)
+    devn = torch.device("cuda", 0)
+    peaks, _ = load_peaks()
+    x = W.make_inputs(wl)
+    T, H, D = wl.total_tokens, wl.n_heads, wl.head_dim
+    q = torch.from_numpy(x["q"]).to(devn)
+    k = torch.from_numpy(x["k"]).to(devn)
+    cu = torch.from_numpy(wl.cu_seqlens).to(devn)
+    g = torch.from_numpy(x["ln_gamma"]).to(devn) if wl.layernorm else None
+    b = torch.from_numpy(x["ln_beta"]).to(devn) if wl.layernorm else None
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=devn)
+    stream = torch.cuda.current_stream()
+    prec = "mxfp8" if wl.prec == "bf16" else wl.prec
+    outs = dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False, True, prec)
+    ms = _median_ms(lambda: dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False,
+                                           True, prec, out=outs), flush, stream)
+    nb = T * H * D * 4 + T * D * 4 + T * H * D + T * H * D // 32 + T * D + T * D // 32
+    line = {"mode": "hbm-kernels", "workload": describe(wl, prec),
+            "preprocess": {"ms": ms, "bytes": nb, "GB/s": nb / ms / 1e6, "frac_of_hbm": nb / ms / 1e6 / peaks["hbm_gbs"]}}
+    line.update(time_hbm_kernels(dsa, q, T, H, D, flush, stream, peaks))
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, wl):
     world, rank, _ = dist_setup(args.gpus)
     if rank != 0:
@@ -598,12 +628,16 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-hbm", action="store_true", help="skip timing the stand-alone HBM-bound kernels")
+    ap.add_argument("--hbm-only", action="store_true",
+                    help="time only the HBM-bound kernels on the workload and print their GB/s")
     ap.add_argument("--table", action="store_true",
                     help="time every configuration and print a markdown table instead of the JSON line")
     args = ap.parse_args()
     wl = W.config(args.workload)
     if args.table:
         run_table(args)
+    elif args.hbm_only:
+        run_hbm_only(args, wl)
     elif args.impl == "reference":
         run_reference(args, wl)
     else:
