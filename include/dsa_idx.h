@@ -66,7 +66,11 @@ typedef enum {
   DSA_ERR_UNSUPPORTED = 2, /* shape / head count / device not supported */
   DSA_ERR_CUDA = 3,        /* a CUDA runtime call failed */
   DSA_ERR_WORKSPACE = 4,   /* workspace missing or too small */
-  DSA_ERR_TIMEOUT = 5      /* a device-side bounded wait gave up */
+  DSA_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up */
+  DSA_ERR_BOUNDS = 6       /* checked build (DSA_CHECKED) only: a device-side
+                              bounds check on a candidate-buffer or output
+                              write failed; the write was skipped (a library
+                              defect, never an input error) */
 } dsa_status_t;
 
 typedef enum { DSA_DTYPE_F32 = 0, DSA_DTYPE_BF16 = 1 } dsa_dtype_t;
@@ -93,6 +97,17 @@ typedef enum { DSA_MX_SCALE_NOSAT = 0, DSA_MX_SCALE_FLOOR = 1 } dsa_mx_scale_rul
  * caller-computed compressed keys, cu_pools their per-document prefix; each
  * query keeps index_topk compressed keys, indices not expanded to tokens. */
 #define DSA_FLAG_COMPRESSED_KEYS 0x8
+
+/* Checked build.  Compiled with -DDSA_CHECKED (libdsa_idx_checked.so, built by
+ * build_lib.build_checked()), the library adds, at some cost in speed:
+ *   - a pass over the inputs of every score + top-k call before the fused
+ *     kernel: a NaN or Inf in q, k (BF16 operands), w, an E4M3 NaN code or a
+ *     UE8M0 NaN scale (0xFF) records DSA_ERR_INVALID_ARG in the status word
+ *     and the call writes no output (reading of the pages' silence on
+ *     non-finite inputs: undefined in the normal build);
+ *   - bounds checks on every candidate-buffer and output write of the fused
+ *     kernel, recording DSA_ERR_BOUNDS and skipping the write.
+ * The entry points and their arguments are the same. */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int dsa_idx_version(void);

@@ -17,6 +17,7 @@ DSA_ERR_UNSUPPORTED = 2
 DSA_ERR_CUDA = 3
 DSA_ERR_WORKSPACE = 4
 DSA_ERR_TIMEOUT = 5
+DSA_ERR_BOUNDS = 6
 # dsa_dtype_t
 DSA_DTYPE_F32 = 0
 DSA_DTYPE_BF16 = 1

@@ -91,5 +91,18 @@ def build(verbose: bool = False, force: bool = False, defines=(), build_dir: str
     return LIB_
 
 
+LIB_CHECKED = os.path.join(PKG, "libdsa_idx_checked.so")
+
+
+def build_checked(verbose: bool = False, force: bool = False) -> str:
+    """The checked build (-DDSA_CHECKED): the same entry points, plus a NaN/Inf
+    scan of every score + top-k call's inputs and device bounds checks on the
+    fused kernel's candidate-buffer and output writes (status word).  A
+    debugging aid and the tests' stand-in for a memory checker; not the
+    product library."""
+    return build(verbose=verbose, force=force, defines=("DSA_CHECKED",), build_dir=BUILD + "_checked",
+                 lib_path=LIB_CHECKED)
+
+
 if __name__ == "__main__":
     build(verbose="-v" in sys.argv, force="-f" in sys.argv)

@@ -148,7 +148,11 @@ int g_fault_inject = 0;
 
 extern "C" {
 
-int dsa_idx_version(void) { return 100; }
+#ifdef DSA_CHECKED
+int dsa_idx_version(void) { return 200 + 1; }   // 2.0.0, checked build (odd)
+#else
+int dsa_idx_version(void) { return 200; }       // 2.0.0
+#endif
 
 const char* dsa_idx_last_error(void) { return g_last_error.c_str(); }
 
@@ -160,6 +164,7 @@ const char* dsa_idx_status_string(dsa_status_t s) {
     case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
     case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
     case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_BOUNDS: return "DSA_ERR_BOUNDS";
   }
   return "DSA_ERR_UNKNOWN";
 }
@@ -381,6 +386,7 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   p.out_idx = topk_idx;
   p.out_score = topk_score;
   p.out_len = topk_len;
+  p.out_rows = total_tokens;
   p.items = items;
   p.hdr = hdr;
   p.tile_base = tile_base;
@@ -402,6 +408,17 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
                                         tile_base, hdr, max_items, st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   if (total_tokens == 0) return DSA_OK;
+#ifdef DSA_CHECKED
+  {
+    const int64_t elem = fp8 ? 1 : 2;
+    const int64_t qrows = (int64_t)total_tokens * n_heads;
+    const int64_t ns = mx ? head_dim / 32 : 1;   // scale bytes per row (FP8: one)
+    e = launch_validate_inputs(q, qrows * head_dim * elem, k, krows * head_dim * elem, fp8 ? 0 : 1,
+                               fp8 ? q_scale : nullptr, qrows * ns, fp8 ? k_scale : nullptr, krows * ns, w,
+                               (int64_t)total_tokens * n_heads, w_dtype == DSA_DTYPE_BF16, hdr, di.sm_count, st);
+    if (e != cudaSuccess) return cuda_fail(e, "input check launch");
+  }
+#endif
   if (mx) {
     e = launch_tiled_kscales(k_scale, krows, p.cu_keys, tile_base, num_seqs,
                              ws_ksf_tiles(ws_tokens, num_seqs), ksf_tiles, di.sm_count, st);

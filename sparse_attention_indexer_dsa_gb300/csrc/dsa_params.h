@@ -51,6 +51,11 @@ cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const i
                                  const int* tile_base, int num_seqs, int max_tiles, uint32_t* out,
                                  int sm_count, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int grid, cudaStream_t stream);
+// Checked build: NaN / Inf scan of a score + top-k call's inputs (status word).
+cudaError_t launch_validate_inputs(const void* q, int64_t q_bytes, const void* k, int64_t k_bytes, int op_bf16,
+                                   const uint8_t* qs, int64_t qs_bytes, const uint8_t* ks, int64_t ks_bytes,
+                                   const void* w, int64_t w_elems, int w_bf16, int* hdr, int sm_count,
+                                   cudaStream_t stream);
 cudaError_t launch_debug_mma_tile(const DebugParams& p, int prec, cudaStream_t stream);
 // Reorders each finished top-k row into ranking order (score desc, index asc),
 // moving units of `group` consecutive entries (1, or the KPool pool size).

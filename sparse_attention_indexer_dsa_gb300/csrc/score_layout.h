@@ -75,6 +75,7 @@ struct ScoreParams {
   int32_t* out_idx;
   float* out_score;
   int32_t* out_len;
+  int64_t out_rows;         // rows of the outputs (query tokens)
   const int2* items;        // device work list
   int* hdr;                 // [0] status, [1] item count
   const int* tile_base;     // first key tile of each document in ksf_tiles

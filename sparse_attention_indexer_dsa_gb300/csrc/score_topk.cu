@@ -61,6 +61,24 @@ __device__ long long g_trace[16][256];
 #define TRACE(ev, t, cond) ((void)0)
 #endif
 
+// Checked build (-DDSA_CHECKED): a write's bounds condition is verified on the
+// device; a failure records DSA_ERR_BOUNDS in the status word and the write is
+// skipped.  In the normal build the conditions hold by construction and cost
+// nothing.
+#ifdef DSA_CHECKED
+__device__ __forceinline__ bool in_bounds(bool ok, int* status) {
+  if (!ok) set_status(status, DSA_DEV_ERR_BOUNDS);
+  return ok;
+}
+#define DSA_IN_BOUNDS(cond, status) in_bounds((cond), (status))
+#define DSA_CHK_PARAM , int* status
+#define DSA_CHK_ARG , status
+#else
+#define DSA_IN_BOUNDS(cond, status) true
+#define DSA_CHK_PARAM
+#define DSA_CHK_ARG
+#endif
+
 // ----------------------------------------------------------------------------
 // Work list: items (document, first query) sorted by descending tile count so
 // the persistent CTAs take the longest items first.  One block.
@@ -204,6 +222,52 @@ __global__ void __launch_bounds__(kWLThreads) build_worklist_kernel(
   if (tid == 0) hdr[1] = total;
 }
 
+// Checked build: a pass over the inputs of a score + top-k call.  A NaN or
+// Inf in a BF16 operand (exponent bits all ones), an E4M3 NaN code (0x7F /
+// 0xFF), a UE8M0 NaN scale (0xFF) or a non-finite head weight records
+// DSA_ERR_INVALID_ARG in the status word and clears the item count, so the
+// fused kernel that follows writes nothing.  Operands are scanned in 16-byte
+// words (their sizes are multiples of 16 bytes), scales byte by byte.
+__global__ void __launch_bounds__(256) validate_inputs_kernel(
+    const uint8_t* __restrict__ q, int64_t q_bytes, const uint8_t* __restrict__ k, int64_t k_bytes, int op_bf16,
+    const uint8_t* __restrict__ qs, int64_t qs_bytes, const uint8_t* __restrict__ ks, int64_t ks_bytes,
+    const void* __restrict__ w, int64_t w_elems, int w_bf16, int* __restrict__ hdr) {
+  bool bad = false;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+  auto words = [&](const uint8_t* base, int64_t bytes) {
+    for (int64_t i = tid * 16; i < bytes; i += nth * 16) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + i));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (op_bf16) {
+          bad |= (u[j] & 0x7F80u) == 0x7F80u || (u[j] & 0x7F800000u) == 0x7F800000u;
+        } else {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) bad |= ((u[j] >> (8 * b)) & 0x7Fu) == 0x7Fu;
+        }
+      }
+    }
+  };
+  auto scale_bytes = [&](const uint8_t* base, int64_t bytes) {
+    for (int64_t i = tid; i < bytes; i += nth) bad |= base[i] == 0xFFu;
+  };
+  words(q, q_bytes);
+  words(k, k_bytes);
+  if (qs) scale_bytes(qs, qs_bytes);
+  if (ks) scale_bytes(ks, ks_bytes);
+  for (int64_t i = tid; i < w_elems; i += nth) {
+    const uint32_t b = w_bf16 ? (uint32_t)reinterpret_cast<const uint16_t*>(w)[i] << 16
+                              : reinterpret_cast<const uint32_t*>(w)[i];
+    bad |= (b & 0x7F800000u) == 0x7F800000u;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) {
+    set_status(hdr, DSA_DEV_ERR_INVALID_ARG);
+    atomicExch(hdr + 1, 0);
+  }
+}
+
 // MXFP8 key scales, laid out once per call in the tcgen05.cp source form: for
 // key tile t of document d (512 bytes at tile_base[d] + t), 16-byte row l holds
 // the 32-bit scale words of the tile's key rows l, l+32, l+64, l+96 (rows past
@@ -333,7 +397,7 @@ __host__ __device__ constexpr int compact_per() { return score_threads(PREC) <= 
 template <int PER>
 __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n, int keep,
                                            bool exact, int cap_after, int wq, uint32_t lane,
-                                           int* hist, int* ms, int bar_id, int* count_out) {
+                                           int* hist, int* ms, int bar_id, int* count_out DSA_CHK_PARAM) {
   const int tid = wq * 32 + (int)lane;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   int e0 = tid;
@@ -470,8 +534,8 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
       const bool e1 = (be[m] >> lane) & 1u;
       const int my_g = gb + __popc(bg[m] & lt);
       const int my_e = eb + __popc(be[m] & lt);
-      const bool kp = g1 || (e1 && my_e < keep_eq);
       const int pos = my_g + (my_e < keep_eq ? my_e : keep_eq);   // kept entries before it
+      const bool kp = (g1 || (e1 && my_e < keep_eq)) && DSA_IN_BOUNDS(pos < n, status);
       st_shared_u32_if(kp, keys_s + 4u * (uint32_t)pos, rk[m]);
       st_shared_u16_if(kp, idx_s + 2u * (uint32_t)pos, ri[m]);
       gb += __popc(bg[m]);
@@ -498,7 +562,7 @@ __device__ __noinline__ uint32_t wg_select(uint32_t* keys, uint16_t* idx, int n,
 template <int PER>
 __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, int n, int keep,
                                                int cap_after, int wq, uint32_t lane, int* ms,
-                                               int bar_id, uint32_t* tau_out, int* count_out) {
+                                               int bar_id, uint32_t* tau_out, int* count_out DSA_CHK_PARAM) {
   const int tid = wq * 32 + (int)lane;
   uint32_t* sbuf = reinterpret_cast<uint32_t*>(ms + MS_SORT);
   uint32_t sk = keys[(int)(((long long)tid * n) >> 7)];
@@ -595,8 +659,8 @@ __device__ __noinline__ bool wg_shrink_sampled(uint32_t* keys, uint16_t* idx, in
     }
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
-      const bool kp = (bk[m] >> lane) & 1u;
       const int pos = base + __popc(bk[m] & lt);
+      const bool kp = ((bk[m] >> lane) & 1u) && DSA_IN_BOUNDS(pos < n, status);
       st_shared_u32_if(kp, keys_s + 4u * (uint32_t)pos, rk[m]);
       st_shared_u16_if(kp, idx_s + 2u * (uint32_t)pos, ri[m]);
       base += __popc(bk[m]);
@@ -1089,8 +1153,9 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
               const int before = (wq > 0 ? cc[b].x : 0) + (wq > 1 ? cc[b].y : 0) + (wq > 2 ? cc[b].z : 0);
-              const bool mine = (bbal[b][qi] >> lane) & 1u;
-              const int pos = qi * C + count[qi] + before + __popc(bbal[b][qi] & rmask);
+              const int rel = count[qi] + before + __popc(bbal[b][qi] & rmask);
+              const bool mine = ((bbal[b][qi] >> lane) & 1u) && DSA_IN_BOUNDS(rel < C, status);
+              const int pos = qi * C + rel;
               st_shared_u32_if(mine, ckey_s + 4u * (uint32_t)pos, bkey[b][qi]);
               st_shared_u16_if(mine, cidx_s + 2u * (uint32_t)pos, (uint16_t)((tb + b) * kTileKeys + orow));
               count[qi] += cc[b].x + cc[b].y + cc[b].z + cc[b].w;
@@ -1132,11 +1197,11 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               int kept;
               uint32_t th;
               if (wg_shrink_sampled<compact_per<PREC>()>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, cap, wq,
-                                    lane, ms, bar_id, &th, &kept)) {
+                                    lane, ms, bar_id, &th, &kept DSA_CHK_ARG)) {
                 tau[qi] = th;
               } else {
                 tau[qi] = wg_select<compact_per<PREC>()>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, false,
-                                    cap, wq, lane, hist, ms, bar_id, &kept);
+                                    cap, wq, lane, hist, ms, bar_id, &kept DSA_CHK_ARG);
               }
               count[qi] = kept;
             }
@@ -1152,7 +1217,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         if (qi < qpw_eff && count[qi] > keep) {
           int kept;
           wg_select<compact_per<PREC>()>(ckey_base + qi * C, cidx_base + qi * C, count[qi], keep, true, keep, wq, lane, hist,
-                    ms, bar_id, &kept);
+                    ms, bar_id, &kept DSA_CHK_ARG);
           count[qi] = kept;
         }
       }
@@ -1161,6 +1226,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
       for (int qi = 0; qi < QPW_MAX; ++qi) {
         const int tq = qbase + qi;
         if (qi >= qpw_eff || tq >= m.L) continue;
+        if (!DSA_IN_BOUNDS((int64_t)a + tq < p.out_rows && count[qi] <= C, status)) continue;
         const size_t orow = (size_t)(a + tq) * W;
         const int n = count[qi];
         const uint32_t* ck = ckey_base + qi * C;
@@ -1322,6 +1388,16 @@ cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const i
   if (grid < 1) grid = 1;
   build_tiled_kscales_kernel<<<grid, 128, 0, stream>>>(reinterpret_cast<const uint32_t*>(k_scale), k_rows,
                                                        cu_keys, tile_base, num_seqs, max_tiles, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_inputs(const void* q, int64_t q_bytes, const void* k, int64_t k_bytes, int op_bf16,
+                                   const uint8_t* qs, int64_t qs_bytes, const uint8_t* ks, int64_t ks_bytes,
+                                   const void* w, int64_t w_elems, int w_bf16, int* hdr, int sm_count,
+                                   cudaStream_t stream) {
+  validate_inputs_kernel<<<sm_count * 4, 256, 0, stream>>>(
+      reinterpret_cast<const uint8_t*>(q), q_bytes, reinterpret_cast<const uint8_t*>(k), k_bytes, op_bf16, qs, qs_bytes,
+      ks, ks_bytes, w, w_elems, w_bf16, hdr);
   return cudaGetLastError();
 }
 

@@ -136,3 +136,18 @@ def test_score_plan_fits_every_supported_shape(lib):
                 assert rc in (_abi.DSA_OK, _abi.DSA_ERR_CUDA, _abi.DSA_ERR_UNSUPPORTED), (prec, D, H, k, rc)
                 if rc == _abi.DSA_ERR_UNSUPPORTED:
                     assert b"no kernel configuration" not in lib.dsa_idx_last_error(), (prec, D, H, k)
+
+
+def test_checked_build_exports_the_same_entry_points():
+    """The checked build (-DDSA_CHECKED, device bounds checks and a NaN/Inf
+    scan of the inputs) compiles, loads without a GPU, exports every declared
+    entry point and reports itself by an odd version number."""
+    path = build_lib.build_checked()
+    chk = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(chk, n), n
+    chk.dsa_idx_version.restype = ctypes.c_int
+    assert chk.dsa_idx_version() % 2 == 1
+    assert _abi.load().dsa_idx_version() % 2 == 0
+    chk.dsa_idx_status_string.restype = ctypes.c_char_p
+    assert chk.dsa_idx_status_string(_abi.DSA_ERR_BOUNDS) == b"DSA_ERR_BOUNDS"
