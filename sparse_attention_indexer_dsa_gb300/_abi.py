@@ -8,7 +8,9 @@ from __future__ import annotations
 import ctypes
 import os
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa_idx.so")
+# DSA_IDX_LIB selects another build of the same ABI (e.g. the checked build,
+# libdsa_idx_checked.so); by default the in-tree product library.
+LIB_PATH = os.environ.get("DSA_IDX_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa_idx.so")
 
 # dsa_status_t
 DSA_OK = 0
