@@ -153,6 +153,18 @@ __global__ void __launch_bounds__(kPreThreads, kPreMinBlocks) preprocess_kernel(
   }
   __syncthreads();
   const int d0 = lane * VEC;
+  // this lane's rotary factors and partner lane, the same for every row of the token
+  float rc[VEC], rs[VEC];
+  const bool rot = half > 0 && d0 < p.rope_dim;
+  const uint32_t rot_mask = __ballot_sync(0xffffffffu, rot);   // the rotary lanes (and their partners)
+  const int src_lane = d0 < half ? lane + half / VEC : (d0 < p.rope_dim ? lane - half / VEC : lane);
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    const int d = d0 + e;
+    const int i = p.interleaved ? (d >> 1) : (d < half ? d : d - half);
+    rc[e] = rot ? s_cos[i] : 1.f;
+    rs[e] = rot ? (p.interleaved || d < half ? -s_sin[i] : s_sin[i]) : 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < kPreMaxRows; ++j) {
     const int r = warp + 8 * j;
@@ -180,33 +192,22 @@ __global__ void __launch_bounds__(kPreThreads, kPreMinBlocks) preprocess_kernel(
         if (!p.rope_fp32) v[e] = bf16_rne(v[e]);
       }
     }
-    if (half > 0) {
+    if (rot) {
+      // rotate-half: v' = v cos -/+ partner sin (sign folded into rs); the partner
+      // value comes from lane +- half/VEC.  Interleaved: pairs (2i, 2i+1) in-lane.
       if (p.interleaved) {
 #pragma unroll
         for (int e = 0; e < VEC; e += 2) {
-          const int d = d0 + e;
-          if (d < p.rope_dim) {
-            const float c = s_cos[d >> 1], s = s_sin[d >> 1];
-            const float a = v[e], b = v[e + 1];
-            v[e] = a * c - b * s;
-            v[e + 1] = b * c + a * s;
-          }
+          const float a = v[e], b = v[e + 1];
+          v[e] = fmaf(a, rc[e], b * rs[e]);          // a cos - b sin
+          v[e + 1] = fmaf(b, rc[e + 1], -a * rs[e + 1]);   // b cos + a sin
         }
       } else {
-        const int lane_shift = half / VEC;
-        const int src = d0 < half ? lane + lane_shift : (d0 < p.rope_dim ? lane - lane_shift : lane);
         float pv[VEC];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) pv[e] = __shfl_sync(0xffffffffu, v[e], src);
-        if (d0 < p.rope_dim) {
+        for (int e = 0; e < VEC; ++e) pv[e] = __shfl_sync(rot_mask, v[e], src_lane);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const int d = d0 + e;
-            const int i = d < half ? d : d - half;
-            const float c = s_cos[i], s = s_sin[i];
-            v[e] = d < half ? v[e] * c - pv[e] * s : v[e] * c + pv[e] * s;
-          }
-        }
+        for (int e = 0; e < VEC; ++e) v[e] = fmaf(v[e], rc[e], pv[e] * rs[e]);
       }
     }
     if (!p.rope_fp32) {
@@ -227,13 +228,8 @@ __global__ void __launch_bounds__(kPreThreads, kPreMinBlocks) preprocess_kernel(
         int sb;
         const uint32_t pay = quant_lane4<8>(v, p.scale_rule, &sb);
         reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
-        const int s1 = __shfl_sync(0xffffffffu, sb, 8), s2 = __shfl_sync(0xffffffffu, sb, 16),
-                  s3 = __shfl_sync(0xffffffffu, sb, 24);
-        if (lane == 0) {
-          uint8_t* sc = is_key ? p.k_scale : p.q_scale;
-          reinterpret_cast<uint32_t*>(sc)[orow] =
-              (uint32_t)sb | ((uint32_t)s1 << 8) | ((uint32_t)s2 << 16) | ((uint32_t)s3 << 24);
-        }
+        // the first lane of each 8-lane block writes the block's scale byte
+        if ((lane & 7) == 0) (is_key ? p.k_scale : p.q_scale)[orow * (D / 32) + (lane >> 3)] = (uint8_t)sb;
       }
     } else {
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + orow * D + d0;
