@@ -67,9 +67,19 @@ __device__ __forceinline__ float exp2_neg(int e) {
 // the block's UE8M0.
 template <int GL>
 __device__ __forceinline__ uint32_t quant_lane4(const float v[4], int rule, int* scale_byte) {
-  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  float amax;
+  if constexpr (GL == 32) {
+    // whole-warp block: magnitudes compare as unsigned integers, one warp
+    // reduction (measured faster than five shuffle steps; for 8-lane blocks a
+    // reduction with a partial mask is slower than three shuffles)
+    uint32_t am = max(max(__float_as_uint(v[0]) & 0x7FFFFFFFu, __float_as_uint(v[1]) & 0x7FFFFFFFu),
+                      max(__float_as_uint(v[2]) & 0x7FFFFFFFu, __float_as_uint(v[3]) & 0x7FFFFFFFu));
+    amax = __uint_as_float(__reduce_max_sync(0xffffffffu, am));
+  } else {
+    amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-  for (int o = 1; o < GL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    for (int o = 1; o < GL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  }
   const int e = mx_exponent(amax, rule);
   const float mul = exp2_neg(e);
   const __nv_fp8x2_storage_t lo =
