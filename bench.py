@@ -433,13 +433,17 @@ def run_native(args, wl):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=devn)
     stream = torch.cuda.current_stream()
 
+    nvtx = torch.cuda.nvtx   # named ranges for nsys/ncu timelines (no effect without a profiler)
+
     def pre():
-        dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False, True,
-                       prec, out=(q_op, q_sc, k_op, k_sc))
+        with nvtx.range("dsa_idx_preprocess"):
+            dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False, True,
+                           prec, out=(q_op, q_sc, k_op, k_sc))
 
     def score():
-        dsa.score_topk(q_op, q_sc, k_op, k_sc, w, cu, wl.max_seqlen, H, K, prec, ws=ws,
-                       out=(idx, sco, lens))
+        with nvtx.range("dsa_idx_score_topk"):
+            dsa.score_topk(q_op, q_sc, k_op, k_sc, w, cu, wl.max_seqlen, H, K, prec, ws=ws,
+                           out=(idx, sco, lens))
 
     for _ in range(args.warmup):
         pre()
@@ -459,11 +463,12 @@ def run_native(args, wl):
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                      # L2 flush, outside the events
-        ev[s][0].record(stream)
-        pre()
-        ev[s][1].record(stream)
-        score()
-        ev[s][2].record(stream)
+        with nvtx.range(f"step {s}"):
+            ev[s][0].record(stream)
+            pre()
+            ev[s][1].record(stream)
+            score()
+            ev[s][2].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
