@@ -280,6 +280,8 @@ def run_table(args):
         orate, _ = oracle_rate(wl, x, prec, n_rows)
         print(f"| {describe(wl, prec)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
               f"{100 * tf / peak:.1f} | {orate:,.1f} ({n_rows}) |", flush=True)
+    print(f"\nPeaks: BF16 {peaks['bf16_tflops']:.1f} TFLOP/s ({peak_kind}); FP8 {fp8_peak:.1f} TFLOP/s "
+          f"(E4M3 GEMM measured in this run) for the MXFP8 and FP8 rows.", flush=True)
 
 
 def _median_ms(fn, flush, stream, reps=5, warm=2):

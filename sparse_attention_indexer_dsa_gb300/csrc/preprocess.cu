@@ -35,52 +35,43 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// UE8M0 exponent of a 32-element block from its max magnitude (see header).
-__device__ __forceinline__ int mx_exponent(float amax, int rule) {
-  const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
-  if (b == 0) return -127;
-  int E;
-  bool above;    // mantissa of amax (normalised) > 1.75
-  const uint32_t eb = b >> 23, mant = b & 0x7FFFFFu;
-  if (eb == 0) {   // subnormal: amax = mant * 2^-149
-    const int pbit = 31 - __clz(mant);
-    E = pbit - 149;
-    above = (uint64_t)mant * 4u > (uint64_t)7u << pbit;
-  } else {
-    E = (int)eb - 127;
-    above = mant > 0x600000u;
-  }
-  int e = rule == 1 ? E - 8 : (above ? E - 7 : E - 8);
-  e = e < -127 ? -127 : (e > 127 ? 127 : e);
-  return e;
+// UE8M0 exponent of a block from the bit pattern of its max magnitude
+// (sign cleared).  With amax = m * 2^E, m in [1, 2), the smallest e with
+// amax <= 448 * 2^e = 1.75 * 2^(e+8) is E - 8, plus one when m > 1.75 (mantissa
+// field above 0x600000).  Adding 0x1FFFFF to the bit pattern carries into the
+// exponent field exactly in that case, so the NOSAT exponent is
+// ((bits + 0x1FFFFF) >> 23) - 135 and the FLOOR exponent (bits >> 23) - 135.
+// Zero, subnormal and tiny magnitudes land at or below -127 and clamp there;
+// the largest pattern (NaN) gives 121, so no upper clamp is needed.
+__device__ __forceinline__ int mx_exponent_bits(uint32_t amax_bits, uint32_t carry) {
+  return max((int)((amax_bits + carry) >> 23) - 135, -127);
 }
 
-// 2^-e as a float for e in [-127, 127]
-__device__ __forceinline__ float exp2_neg(int e) {
-  const int be = 127 - e;
-  return be >= 1 ? __uint_as_float((uint32_t)be << 23) : __uint_as_float(0x00400000u);
-}
+// mantissa carry for the rule: 0 = NOSAT, 1 = FLOOR
+__device__ __forceinline__ uint32_t mx_carry(int rule) { return rule == 1 ? 0u : 0x1FFFFFu; }
+
+// 2^-e as a float for e in [-127, 121] (always a normal number)
+__device__ __forceinline__ float exp2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
 
 // Quantise one block of 4*GL elements spread over GL consecutive lanes (4
 // values per lane): GL = 8 is an MXFP8 block of 32, GL = 32 a whole 128-element
 // row of per-vector FP8.  Returns the lane's 4 payload bytes; *scale_byte is
 // the block's UE8M0.
 template <int GL>
-__device__ __forceinline__ uint32_t quant_lane4(const float v[4], int rule, int* scale_byte) {
-  float amax;
+__device__ __forceinline__ uint32_t quant_lane4(const float v[4], uint32_t carry, int* scale_byte) {
+  // magnitudes compare as unsigned integers
+  uint32_t am = max(max(__float_as_uint(v[0]) & 0x7FFFFFFFu, __float_as_uint(v[1]) & 0x7FFFFFFFu),
+                    max(__float_as_uint(v[2]) & 0x7FFFFFFFu, __float_as_uint(v[3]) & 0x7FFFFFFFu));
   if constexpr (GL == 32) {
-    // whole-warp block: magnitudes compare as unsigned integers, one warp
-    // reduction (measured faster than five shuffle steps; for 8-lane blocks a
-    // reduction with a partial mask is slower than three shuffles)
-    uint32_t am = max(max(__float_as_uint(v[0]) & 0x7FFFFFFFu, __float_as_uint(v[1]) & 0x7FFFFFFFu),
-                      max(__float_as_uint(v[2]) & 0x7FFFFFFFu, __float_as_uint(v[3]) & 0x7FFFFFFFu));
-    amax = __uint_as_float(__reduce_max_sync(0xffffffffu, am));
+    // whole-warp block: one warp reduction (measured faster than five shuffle
+    // steps; for 8-lane blocks a reduction with a partial mask is slower than
+    // three shuffles)
+    am = __reduce_max_sync(0xffffffffu, am);
   } else {
-    amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-    for (int o = 1; o < GL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    for (int o = 1; o < GL; o <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
   }
-  const int e = mx_exponent(amax, rule);
+  const int e = mx_exponent_bits(am, carry);
   const float mul = exp2_neg(e);
   const __nv_fp8x2_storage_t lo =
       __nv_cvt_float2_to_fp8x2(make_float2(v[0] * mul, v[1] * mul), __NV_SATFINITE, __NV_E4M3);
@@ -120,70 +111,185 @@ __device__ __forceinline__ void load_row(const void* base, int in_bf16, size_t r
 
 constexpr int kPreThreads = 256;
 constexpr int kPreMinBlocks = 4;   // resident blocks per SM: 64 registers a thread, no spills
-constexpr int kPreMaxRows = 9;   // ceil((64 query heads + 1 key) / 8 warps)
+constexpr int kPreQRows = 8;       // query rows per warp: H <= 64 over 8 warps
 
-// One block per token.  Row r < H is query head r, row H is the key.
-template <int D>
+enum PreRope { kRopeNone = 0, kRopeHalf = 1, kRopeInterleaved = 2 };
+
+// Loads row `row` of a [rows, D] tensor, VEC = D/32 values per lane.
+template <int VEC, bool IN_BF16>
+__device__ __forceinline__ void load_lane(const void* base, size_t row, int lane, float (&x)[VEC]) {
+  constexpr int D = VEC * 32;
+  if constexpr (IN_BF16) {
+    const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(base) + row * D + lane * VEC;
+    if constexpr (VEC == 4) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+      x[0] = __uint_as_float(u.x << 16);
+      x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(u.y << 16);
+      x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(p));
+      x[0] = __uint_as_float(u << 16);
+      x[1] = __uint_as_float(u & 0xFFFF0000u);
+    }
+  } else {
+    const float* p = reinterpret_cast<const float*>(base) + row * D + lane * VEC;
+    if constexpr (VEC == 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+      x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    } else {
+      const float2 f = __ldg(reinterpret_cast<const float2*>(p));
+      x[0] = f.x; x[1] = f.y;
+    }
+  }
+}
+
+// The issued loads of one token: up to 8 query rows per warp plus the key row
+// (held by warp H % 8).
+template <int VEC, bool IN_BF16>
+__device__ __forceinline__ void load_token(const PreParams& p, int t, int warp, int lane,
+                                           float (&xq)[kPreQRows][VEC], float (&xk)[VEC]) {
+  const int H = p.H;
+#pragma unroll
+  for (int j = 0; j < kPreQRows; ++j) {
+    const int r = warp + 8 * j;
+    if (r < H) load_lane<VEC, IN_BF16>(p.q, (size_t)t * H + r, lane, xq[j]);
+  }
+  if (warp == (H & 7)) load_lane<VEC, IN_BF16>(p.k, (size_t)t, lane, xk);
+}
+
+// RoPE (in-place) for one row; rc/rs are the lane's rotary factors (1 and 0
+// on unrotated dims) with the rotate-half sign folded into rs.
+template <int VEC, int ROPE>
+__device__ __forceinline__ void rope_row(float (&v)[VEC], const float (&rc)[VEC], const float (&rs)[VEC],
+                                         bool rot, int src_lane) {
+  if constexpr (ROPE == kRopeHalf) {
+    // partner value from lane +- half/VEC (itself on unrotated lanes)
+    float pv[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) pv[e] = __shfl_sync(0xffffffffu, v[e], src_lane);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const float r = fmaf(v[e], rc[e], pv[e] * rs[e]);
+      v[e] = rot ? r : v[e];
+    }
+  } else if constexpr (ROPE == kRopeInterleaved) {
+    // pairs (2i, 2i+1) in-lane: (a cos - b sin, b cos + a sin)
+#pragma unroll
+    for (int e = 0; e < VEC; e += 2) {
+      const float a = v[e], b = v[e + 1];
+      const float ra = fmaf(a, rc[e], b * rs[e]);
+      const float rb = fmaf(b, rc[e + 1], -a * rs[e + 1]);
+      v[e] = rot ? ra : a;
+      v[e + 1] = rot ? rb : b;
+    }
+  }
+}
+
+// Quantises (or rounds) one finished row and stores it.
+template <int VEC, int OUT>
+__device__ __forceinline__ void store_row(const float (&v)[VEC], void* out, uint8_t* scale, size_t orow,
+                                          int lane, uint32_t carry) {
+  constexpr int D = VEC * 32;
+  if constexpr (OUT == 2) {   // FP8, one scale per row (D = 128: 4 values per lane)
+    int sb;
+    const uint32_t pay = quant_lane4<32>(v, carry, &sb);
+    reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
+    if (lane == 0) scale[orow] = (uint8_t)sb;
+  } else if constexpr (OUT == 1) {   // MXFP8, one scale per 32 elements (8 lanes)
+    int sb;
+    const uint32_t pay = quant_lane4<8>(v, carry, &sb);
+    reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
+    // the first lane of each 8-lane block writes the block's scale byte
+    if ((lane & 7) == 0) scale[orow * (D / 32) + (lane >> 3)] = (uint8_t)sb;
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + orow * D + lane * VEC;
+    if constexpr (VEC == 4) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&a);
+      u.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(o) = u;
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(v[0], v[1]);
+    }
+  }
+}
+
+// One block per token: warp w handles query heads w, w+8, ... and warp H % 8
+// also the key row.  Every choice that is fixed for a call (output format,
+// RoPE layout, BF16 rounding between the steps) is a template parameter, so a
+// row's code has no branches.
+template <int D, int OUT, int ROPE, bool MID_BF16>
 __global__ void __launch_bounds__(kPreThreads, kPreMinBlocks) preprocess_kernel(const __grid_constant__ PreParams p) {
   constexpr int VEC = D / 32;
   __shared__ float s_cos[64], s_sin[64];
-  __shared__ int s_pos;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H;
   // issue the row loads first (memory-level parallelism), then the position
-  float x[kPreMaxRows][VEC];
-#pragma unroll
-  for (int j = 0; j < kPreMaxRows; ++j) {
-    const int r = warp + 8 * j;
-    if (r < H) load_row<VEC>(p.q, p.in_bf16, (size_t)t * H + r, D, lane, x[j]);
-    else if (r == H) load_row<VEC>(p.k, p.in_bf16, (size_t)t, D, lane, x[j]);
-  }
-  if (threadIdx.x == 0) {
-    int lo = 0, hi = p.num_seqs - 1;   // last document whose start is <= t
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.cu[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    s_pos = t - p.cu[lo];
-  }
-  __syncthreads();
-  const int half = p.rope_dim >> 1;
-  if ((int)threadIdx.x < half) {
-    // angle pos*theta_i in double, Cody-Waite reduction by 2*pi (two-term
-    // constant), then single-precision sincos of the reduced angle
-    const double ang = (double)s_pos * p.inv_freq[threadIdx.x];
-    const double kq = rint(ang * 0.15915494309189535);
-    double red = fma(-kq, 6.283185307179586, ang);
-    red = fma(-kq, 2.4492935982947064e-16, red);
-    float sv, cv;
-    sincosf((float)red, &sv, &cv);
-    s_cos[threadIdx.x] = cv;
-    s_sin[threadIdx.x] = sv;
-  }
-  __syncthreads();
-  const int d0 = lane * VEC;
-  // this lane's rotary factors and partner lane, the same for every row of the token
+  float xq[kPreQRows][VEC], xk[VEC];
+  if (p.in_bf16) load_token<VEC, true>(p, t, warp, lane, xq, xk);
+  else load_token<VEC, false>(p, t, warp, lane, xq, xk);
   float rc[VEC], rs[VEC];
-  const bool rot = half > 0 && d0 < p.rope_dim;
-  const uint32_t rot_mask = __ballot_sync(0xffffffffu, rot);   // the rotary lanes (and their partners)
-  const int src_lane = d0 < half ? lane + half / VEC : (d0 < p.rope_dim ? lane - half / VEC : lane);
+  bool rot = false;
+  int src_lane = lane;
+  if constexpr (ROPE != kRopeNone) {
+    const int half = p.rope_dim >> 1;
+    if (warp == 0) {
+      // position in the document: every lane of warp 0 runs the same search
+      int lo = 0, hi = p.num_seqs - 1;   // last document whose start is <= t
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.cu + mid) <= t) lo = mid; else hi = mid - 1;
+      }
+      const int pos = t - __ldg(p.cu + lo);
+      for (int i = lane; i < half; i += 32) {
+        // angle pos*theta_i in double, Cody-Waite reduction by 2*pi (two-term
+        // constant), then single-precision sincos of the reduced angle
+        const double ang = (double)pos * p.inv_freq[i];
+        const double kq = rint(ang * 0.15915494309189535);
+        double red = fma(-kq, 6.283185307179586, ang);
+        red = fma(-kq, 2.4492935982947064e-16, red);
+        float sv, cv;
+        sincosf((float)red, &sv, &cv);
+        s_cos[i] = cv;
+        s_sin[i] = sv;
+      }
+    }
+    __syncthreads();
+    // this lane's rotary factors and partner lane, the same for every row
+    const int d0 = lane * VEC;
+    rot = d0 < p.rope_dim;
+    if constexpr (ROPE == kRopeHalf)
+      src_lane = d0 < half ? lane + half / VEC : (rot ? lane - half / VEC : lane);
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) {
-    const int d = d0 + e;
-    const int i = p.interleaved ? (d >> 1) : (d < half ? d : d - half);
-    rc[e] = rot ? s_cos[i] : 1.f;
-    rs[e] = rot ? (p.interleaved || d < half ? -s_sin[i] : s_sin[i]) : 0.f;
+    for (int e = 0; e < VEC; ++e) {
+      const int d = d0 + e;
+      const int i = ROPE == kRopeInterleaved ? (d >> 1) : (d < half ? d : d - half);
+      const int ic = rot ? i : 0;
+      rc[e] = rot ? s_cos[ic] : 1.f;
+      rs[e] = rot ? (ROPE == kRopeInterleaved || d < half ? -s_sin[ic] : s_sin[ic]) : 0.f;
+    }
   }
+  const uint32_t carry = mx_carry(p.scale_rule);
+  uint8_t* q_scale = p.q_scale;
+  void* q_out = p.q_out;
 #pragma unroll
-  for (int j = 0; j < kPreMaxRows; ++j) {
+  for (int j = 0; j < kPreQRows; ++j) {
     const int r = warp + 8 * j;
-    if (r > H) break;
-    const bool is_key = r == H;
-    float v[VEC];
+    if (r >= H) break;
+    rope_row<VEC, ROPE>(xq[j], rc, rs, rot, src_lane);
+    if constexpr (MID_BF16) {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) v[e] = x[j][e];
-    if (is_key && p.gamma != nullptr) {   // key LayerNorm: biased variance, two passes
+      for (int e = 0; e < VEC; ++e) xq[j][e] = bf16_rne(xq[j][e]);
+    }
+    store_row<VEC, OUT>(xq[j], q_out, q_scale, (size_t)t * H + r, lane, carry);
+  }
+  if (warp == (H & 7)) {
+    float* v = xk;
+    if (p.gamma != nullptr) {   // key LayerNorm: biased variance, two passes
       float s = 0.f;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) s += v[e];
@@ -198,62 +304,16 @@ __global__ void __launch_bounds__(kPreThreads, kPreMinBlocks) preprocess_kernel(
       const float rstd = 1.0f / sqrtf(var + p.eps);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        v[e] = fmaf(v[e] * rstd, __ldg(p.gamma + d0 + e), __ldg(p.beta + d0 + e));
-        if (!p.rope_fp32) v[e] = bf16_rne(v[e]);
+        v[e] = fmaf(v[e] * rstd, __ldg(p.gamma + lane * VEC + e), __ldg(p.beta + lane * VEC + e));
+        if constexpr (MID_BF16) v[e] = bf16_rne(v[e]);
       }
     }
-    if (rot) {
-      // rotate-half: v' = v cos -/+ partner sin (sign folded into rs); the partner
-      // value comes from lane +- half/VEC.  Interleaved: pairs (2i, 2i+1) in-lane.
-      if (p.interleaved) {
+    rope_row<VEC, ROPE>(xk, rc, rs, rot, src_lane);
+    if constexpr (MID_BF16) {
 #pragma unroll
-        for (int e = 0; e < VEC; e += 2) {
-          const float a = v[e], b = v[e + 1];
-          v[e] = fmaf(a, rc[e], b * rs[e]);          // a cos - b sin
-          v[e + 1] = fmaf(b, rc[e + 1], -a * rs[e + 1]);   // b cos + a sin
-        }
-      } else {
-        float pv[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) pv[e] = __shfl_sync(rot_mask, v[e], src_lane);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) v[e] = fmaf(v[e], rc[e], pv[e] * rs[e]);
-      }
+      for (int e = 0; e < VEC; ++e) xk[e] = bf16_rne(xk[e]);
     }
-    if (!p.rope_fp32) {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) v[e] = bf16_rne(v[e]);
-    }
-    const size_t orow = is_key ? (size_t)t : (size_t)t * H + r;
-    void* out = is_key ? p.k_out : p.q_out;
-    if (p.out_mode == 2) {   // FP8, one scale per row (D = 128: 4 values per lane)
-      if constexpr (VEC == 4) {
-        int sb;
-        const uint32_t pay = quant_lane4<32>(v, p.scale_rule, &sb);
-        reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
-        if (lane == 0) (is_key ? p.k_scale : p.q_scale)[orow] = (uint8_t)sb;
-      }
-    } else if (p.out_mode == 1) {
-      if constexpr (VEC == 4) {
-        int sb;
-        const uint32_t pay = quant_lane4<8>(v, p.scale_rule, &sb);
-        reinterpret_cast<uint32_t*>(out)[orow * (D / 4) + lane] = pay;
-        // the first lane of each 8-lane block writes the block's scale byte
-        if ((lane & 7) == 0) (is_key ? p.k_scale : p.q_scale)[orow * (D / 32) + (lane >> 3)] = (uint8_t)sb;
-      }
-    } else {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + orow * D + d0;
-      if constexpr (VEC == 4) {
-        __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
-        __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&a);
-        u.y = *reinterpret_cast<uint32_t*>(&b);
-        *reinterpret_cast<uint2*>(o) = u;
-      } else {
-        *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(v[0], v[1]);
-      }
-    }
+    store_row<VEC, OUT>(xk, p.k_out, p.k_scale, (size_t)t, lane, carry);
   }
 }
 
@@ -285,7 +345,7 @@ __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const void* __restr
       }
     }
     int sb;
-    const uint32_t pay = quant_lane4<8>(v, rule, &sb);
+    const uint32_t pay = quant_lane4<8>(v, mx_carry(rule), &sb);
     if (valid) {
       reinterpret_cast<uint32_t*>(out)[e0 >> 2] = pay;
       if ((lane & 7) == 0) scales[blk] = (uint8_t)sb;
@@ -304,7 +364,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_rows_kernel(const void* __re
     float v[4];
     load_row<4>(x, in_bf16, (size_t)r, 128, lane, v);
     int sb;
-    const uint32_t pay = quant_lane4<32>(v, rule, &sb);
+    const uint32_t pay = quant_lane4<32>(v, mx_carry(rule), &sb);
     reinterpret_cast<uint32_t*>(out)[r * 32 + lane] = pay;
     if (lane == 0) scales[r] = (uint8_t)sb;
   }
@@ -320,12 +380,30 @@ cudaError_t launch_quantize_fp8_rows(const void* x, int in_bf16, int64_t rows, i
   return cudaGetLastError();
 }
 
+template <int D, int OUT, int ROPE>
+static void launch_pre_mid(const PreParams& p, cudaStream_t stream) {
+  if (p.rope_fp32)
+    preprocess_kernel<D, OUT, ROPE, false><<<p.total_tokens, kPreThreads, 0, stream>>>(p);
+  else
+    preprocess_kernel<D, OUT, ROPE, true><<<p.total_tokens, kPreThreads, 0, stream>>>(p);
+}
+
+template <int D, int OUT>
+static void launch_pre_rope(const PreParams& p, cudaStream_t stream) {
+  if (p.rope_dim == 0) launch_pre_mid<D, OUT, kRopeNone>(p, stream);
+  else if (p.interleaved) launch_pre_mid<D, OUT, kRopeInterleaved>(p, stream);
+  else launch_pre_mid<D, OUT, kRopeHalf>(p, stream);
+}
+
 cudaError_t launch_preprocess(const PreParams& p, int D, cudaStream_t stream) {
   if (p.total_tokens == 0) return cudaSuccess;
-  if (D == 128)
-    preprocess_kernel<128><<<p.total_tokens, kPreThreads, 0, stream>>>(p);
-  else
-    preprocess_kernel<64><<<p.total_tokens, kPreThreads, 0, stream>>>(p);
+  if (D == 128) {
+    if (p.out_mode == 1) launch_pre_rope<128, 1>(p, stream);
+    else if (p.out_mode == 2) launch_pre_rope<128, 2>(p, stream);
+    else launch_pre_rope<128, 0>(p, stream);
+  } else {
+    launch_pre_rope<64, 0>(p, stream);   // 64-wide rows: BF16 output only
+  }
   return cudaGetLastError();
 }
 
