@@ -150,3 +150,32 @@ def test_score_order_key_offsets_integer_exact():
     torch.cuda.synchronize()
     ref = O.indexer_topk(q, kk, w.astype(np.float64), cq, k, order="score", cu_seqlens_k=ck)
     _check_exact(g, ref)
+
+
+@pytest.mark.parametrize("outlier", [1.0, 20.0, 2.0 ** 20])
+@pytest.mark.parametrize("k", [700, 2048, 3000])
+def test_score_order_spread_and_crowded_rows(outlier, k):
+    """Float operands with 1 % of the keys scaled by `outlier`: at 1 and 20 the
+    rows' scores spread over the buckets of the ranking pass (its bucket rank),
+    at 2^20 the other scores crowd into one bucket and the rows take the radix
+    fallback.  Either way the ranking-order row must be the index-order row
+    ordered by the GPU's own scores, ties to the lower index."""
+    rng = np.random.default_rng(int(outlier) % 1000 + k)
+    lens, H, D = [k + 900, 300], 32, 128
+    T = sum(lens)
+    kv = rng.standard_normal((T, D))
+    kv[rng.random(T) < 0.01] *= outlier
+    qc, qs, _ = O.quantize_mxfp8(rng.standard_normal((T * H, D)))
+    kc, ks, _ = O.quantize_mxfp8(kv)
+    w = (rng.standard_normal((T, H)) * 0.125).astype(np.float32)
+    cu = dev(np.array([0, lens[0], T], np.int32))
+    ops = (dev(qc), dev(qs), dev(kc), dev(ks), dev(w), cu, max(lens), H, k, "mxfp8")
+    ia, sa, la = (host(t) for t in dsa.score_topk(*ops))
+    ib, sb, lb = (host(t) for t in dsa.score_topk(*ops, order="score"))
+    np.testing.assert_array_equal(la, lb)
+    for t in range(T):
+        n = int(la[t])
+        perm = np.lexsort((ia[t, :n], -sa[t, :n].astype(np.float64)))
+        np.testing.assert_array_equal(ib[t, :n], ia[t, :n][perm], err_msg=f"row {t}")
+        np.testing.assert_array_equal(sb[t, :n], sa[t, :n][perm], err_msg=f"row {t}")
+        assert (ib[t, n:] == -1).all() and np.isneginf(sb[t, n:]).all()
