@@ -572,6 +572,24 @@ def run_native(args, wl):
 
     hbm_kernels = None if args.no_hbm else time_hbm_kernels(dsa, q, T, H, D, flush, stream, peaks)
 
+    # the ranking-order pass (DSA_FLAG_SORT_BY_SCORE): the same call in score
+    # order against index order on the same operands, medians of 5 (L2 flushed)
+    ranking = None
+    if not args.no_rank:
+        def call(order):
+            return lambda: dsa.score_topk(q_op, q_sc, k_op, k_sc, w, cu, wl.max_seqlen, H, K, prec, ws=ws,
+                                          out=(idx, sco, lens), order=order)
+        ms_idx = _median_ms(call("index"), flush, stream)
+        ms_score = _median_ms(call("score"), flush, stream)
+        rows_bytes = 2 * T * K * 8                      # each row read and written once (index + score)
+        extra = ms_score - ms_idx
+        ranking = {"index_order_ms": ms_idx, "score_order_ms": ms_score, "ranking_pass_ms": extra,
+                   "rows": T, "width": K, "bytes": rows_bytes,
+                   "GB/s": rows_bytes / extra / 1e6 if extra > 0 else None}
+        st = dsa.read_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the ranking-order calls")
+
     if rank != 0:
         return
     flops = wl.flops()
@@ -605,6 +623,7 @@ def run_native(args, wl):
                      "traffic_source": tr["scaled_to"] if tr else None},
         "bf16_scoring": bf16,
         "hbm_kernels": hbm_kernels,
+        "ranking_order": ranking,
         "e2e": {"value": job_rate(world, T, 1, e2e_ms), "unit": "queries/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host q,k,w -> dsa_idx_preprocess -> dsa_idx_score_topk -> host top-k indices; "
@@ -635,6 +654,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-hbm", action="store_true", help="skip timing the stand-alone HBM-bound kernels")
+    ap.add_argument("--no-rank", action="store_true", help="skip timing the ranking-order pass")
     ap.add_argument("--hbm-only", action="store_true",
                     help="time only the HBM-bound kernels on the workload and print their GB/s")
     ap.add_argument("--table", action="store_true",
