@@ -220,8 +220,10 @@ dsa_status_t dsa_idx_kpool_compress(
  *   index_topk  keys selected per query; in pool mode a multiple of
  *               kpool_size, and index_topk / kpool_size pools are kept
  *   prec     BF16 (kind::f16), MXFP8 (block-scaled kind::mxf8f6f4) or FP8
- *            (kind::f8f6f4; the per-row scales are folded exactly into the
- *            head weights and the key's score, as powers of two)
+ *            (the same block-scaled MMA with each key row's one scale
+ *            repeated over its four 32-element blocks; the query rows'
+ *            scales are folded exactly into the head weights, as powers of
+ *            two)
  *   flags    DSA_FLAG_* bits
  *   kpool_size  1 = plain keys; >1 = pool mode (cu_pools required): KPool
  *               pools of that size (2, 4 or 8), or with

@@ -127,8 +127,8 @@ bool heads_ok(int H) { return H == 4 || H == 8 || H == 16 || H == 32 || H == 64;
 
 // workspace layout: [0,256) header (status, item count); per-document item
 // prefix int[num_seqs+1]; per-document key-tile prefix int[num_seqs+1]; work
-// items int2[total_tokens + num_seqs]; MXFP8 only: key scales laid out per
-// key tile, 512 bytes x (total_tokens/128 + num_seqs + 1).
+// items int2[total_tokens + num_seqs]; MXFP8 and FP8: key scales laid out per
+// key tile for tcgen05.cp, 512 bytes x (total_tokens/128 + num_seqs + 1).
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 size_t ws_prefix_off() { return 256; }
 size_t ws_tiles_off(int num_seqs) { return ws_prefix_off() + round256((size_t)(num_seqs + 1) * 4); }
@@ -137,8 +137,9 @@ size_t ws_ksf_off(int total_tokens, int num_seqs) {
   return ws_items_off(num_seqs) + round256((size_t)8 * ((size_t)total_tokens + num_seqs));
 }
 int ws_ksf_tiles(int total_tokens, int num_seqs) { return total_tokens / kTileKeys + num_seqs + 1; }
-size_t ws_total(int total_tokens, int num_seqs, bool mx) {
-  return ws_ksf_off(total_tokens, num_seqs) + (mx ? (size_t)kSfTxBytes * ws_ksf_tiles(total_tokens, num_seqs) : 0);
+size_t ws_total(int total_tokens, int num_seqs, bool scales) {
+  return ws_ksf_off(total_tokens, num_seqs) +
+         (scales ? (size_t)kSfTxBytes * ws_ksf_tiles(total_tokens, num_seqs) : 0);
 }
 
 unsigned long long g_timeout_ns = 2000000000ull;
@@ -173,7 +174,7 @@ size_t dsa_idx_workspace_size(int total_tokens, int num_seqs, int max_seqlen, in
                               int head_dim, int index_topk, int kpool_size, dsa_precision_t prec) {
   (void)max_seqlen; (void)n_heads; (void)head_dim; (void)index_topk; (void)kpool_size;
   if (total_tokens < 0 || num_seqs < 1) return 0;
-  return ws_total(total_tokens, num_seqs, prec == DSA_PREC_MXFP8);
+  return ws_total(total_tokens, num_seqs, prec == DSA_PREC_MXFP8 || prec == DSA_PREC_FP8);
 }
 
 int dsa_idx_output_width(int index_topk, int kpool_size, int flags) {
@@ -349,7 +350,7 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   const int keep = index_topk / expand;
   if (keep < 1) return fail(DSA_ERR_INVALID_ARG, "index_topk / kpool_size must be >= 1");
   if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
-  const bool mxw = prec == DSA_PREC_MXFP8;
+  const bool mxw = prec == DSA_PREC_MXFP8 || prec == DSA_PREC_FP8;   // key-scale tiles in the workspace
   const int ws_tokens = total_k > total_tokens ? total_k : total_tokens;   // workspace sizing unit
   if (ws_bytes < ws_total(ws_tokens, num_seqs, mxw))
     return fail(DSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, ws_total(ws_tokens, num_seqs, mxw));
@@ -390,9 +391,8 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
   p.items = items;
   p.hdr = hdr;
   p.tile_base = tile_base;
-  p.ksf_tiles = mx ? ksf_tiles : nullptr;
+  p.ksf_tiles = fp8 ? ksf_tiles : nullptr;
   p.q_scale_vec = pl_prec == PREC_FP8 ? q_scale : nullptr;
-  p.k_scale_vec = pl_prec == PREC_FP8 ? k_scale : nullptr;
   p.k_rows = krows;
   p.timeout_ns = g_timeout_ns;
   p.sm_scale = sm_scale;
@@ -419,8 +419,8 @@ dsa_status_t score_topk_impl(const void* q, const uint8_t* q_scale, const void* 
     if (e != cudaSuccess) return cuda_fail(e, "input check launch");
   }
 #endif
-  if (mx) {
-    e = launch_tiled_kscales(k_scale, krows, p.cu_keys, tile_base, num_seqs,
+  if (fp8) {   // FP8: each row's one scale byte, replicated over its four 32-element blocks
+    e = launch_tiled_kscales(k_scale, krows, mx ? 0 : 1, p.cu_keys, tile_base, num_seqs,
                              ws_ksf_tiles(ws_tokens, num_seqs), ksf_tiles, di.sm_count, st);
     if (e != cudaSuccess) return cuda_fail(e, "key-scale layout launch");
   }

@@ -183,17 +183,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
 }
 
 // Block-scaled E4M3 x E4M3 with UE8M0 scales per 32 elements of K (scale_vec::1X)
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f8f6f4 (E4M3 operands, FP32 accumulate)
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                          uint32_t accumulate) {
@@ -336,13 +325,6 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t tile_base, uint32
 // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
-// Instruction descriptor, kind::f8f6f4 (no block scale): D = F32 (bits 4-5 =
-// 1), A = B = E4M3 (format 0 at bits 7-9 and 10-12), both K-major, N >> 3 at
-// bits 17-22, M >> 4 at 24-28.
-__host__ __device__ constexpr uint32_t idesc_f8(uint32_t M, uint32_t N) {
-  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: B scale-factor id at

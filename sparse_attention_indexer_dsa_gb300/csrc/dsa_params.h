@@ -47,7 +47,7 @@ cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, const 
                                   int total_k, int max_seqlen, int max_seqlen_k, int tq, int pool,
                                   int2* items, int* doc_prefix, int* tile_base, int* hdr, int max_items,
                                   cudaStream_t stream);
-cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const int32_t* cu_keys,
+cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, int replicate, const int32_t* cu_keys,
                                  const int* tile_base, int num_seqs, int max_tiles, uint32_t* out,
                                  int sm_count, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int grid, cudaStream_t stream);

@@ -56,7 +56,7 @@ struct ScorePlan {
   int nst;       // K-tile smem stages
   int chunks;    // 128-byte chunks per operand row: head_dim*elem/128
   int qchunk;    // bytes of one q-operand chunk: ncols rows x 128 bytes (TMA box of the q map)
-  int sfb_atoms; // MXFP8: 128-row groups of query scales (ceil(ncols / 128))
+  int sfb_atoms; // MXFP8, FP8: 128-row groups of query scales (ceil(ncols / 128))
   // byte offsets into dynamic shared memory (base 1024-aligned)
   int q_off, k_off, sfa_raw_off, sfa_tx_off, sfb_raw_off, sfb_tx_off;
   int cand_key_off, cand_idx_off, w_off, hist_off, misc_off, bar_off, total;
@@ -79,9 +79,8 @@ struct ScoreParams {
   const int2* items;        // device work list
   int* hdr;                 // [0] status, [1] item count
   const int* tile_base;     // first key tile of each document in ksf_tiles
-  const uint32_t* ksf_tiles;   // MXFP8: key scales laid out per key tile for tcgen05.cp (512 B each)
+  const uint32_t* ksf_tiles;   // MXFP8, FP8: key scales laid out per key tile for tcgen05.cp (512 B each)
   const uint8_t* q_scale_vec;  // FP8: one UE8M0 byte per q row [T*H]
-  const uint8_t* k_scale_vec;  // FP8: one UE8M0 byte per key row
   int64_t k_rows;              // rows of the key operand
   unsigned long long timeout_ns;
   float sm_scale;
@@ -103,6 +102,7 @@ inline int min_stages(int prec, int chunks) { return prec == PREC_BF16 ? 2 * chu
 // Lays out shared memory for (qpw, cand, nst); returns the total bytes.
 inline int layout_score_plan(ScorePlan* s, int nst) {
   const bool sf = s->prec == PREC_MXFP8;
+  const bool f8 = s->prec == PREC_FP8;   // key scales per stage; one tile of unit query scales
   int off = 0;
   s->q_off = off;
   off += s->chunks * s->qchunk;
@@ -111,11 +111,11 @@ inline int layout_score_plan(ScorePlan* s, int nst) {
   off += nst * kStageBytes;
   s->sfa_raw_off = off;   // unused: key scales arrive already laid out for tcgen05.cp
   s->sfa_tx_off = off;
-  off += sf ? nst * kSfTxBytes : 0;
+  off += sf || f8 ? nst * kSfTxBytes : 0;
   s->sfb_raw_off = off;
   off += sf ? 2 * kSfRawBytes : 0;
   s->sfb_tx_off = off;
-  off += sf ? 2 * kSfTxBytes : 0;
+  off += sf ? 2 * kSfTxBytes : (f8 ? kSfTxBytes : 0);
   s->cand_key_off = off;
   off += s->nq * s->cand * 4;
   s->cand_idx_off = off;
@@ -158,7 +158,7 @@ inline bool make_score_plan(int prec, int head_dim, int n_heads, int keep, Score
     s.ncols = s.nq * n_heads;
     if (s.ncols < 16 || s.ncols % 16 != 0 || s.ncols > max_ncols(prec)) return false;
     s.qchunk = s.ncols * kChunkBytes;   // multiple of 1024: keeps the swizzle atoms aligned
-    s.sfb_atoms = sf ? (s.ncols + 127) / 128 : 0;
+    s.sfb_atoms = sf || prec == PREC_FP8 ? (s.ncols + 127) / 128 : 0;
     for (int nmin = min_stages(prec, s.chunks); nmin >= 2; --nmin) {
       // the largest buffer that fits beside nmin stages
       s.cand = 0;

@@ -18,8 +18,9 @@
 //     stage also brings the tile's key scales, laid out for tcgen05.cp.
 //   * Warp 1 issues one tcgen05.mma chain per key tile (M = 128 keys, N = nq*H,
 //     K = head_dim) into a double-buffered TMEM accumulator: kind::f16 (BF16),
-//     block-scaled kind::mxf8f6f4 (MXFP8) or kind::f8f6f4 (FP8, one scale per
-//     row, folded into the epilogue).
+//     block-scaled kind::mxf8f6f4 (MXFP8; FP8 with one scale per row uses it
+//     too, the key row's scale repeated over its blocks and the query row's
+//     folded into the head weights).
 //   * Warps 2.. are the epilogue warpgroups (3, or 4 for BF16), one query
 //     each.  They read the accumulator with tcgen05.ld (16x256b fragments at 64
 //     heads, so each lane needs only 16 head weights), apply ReLU, the head
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(256) validate_inputs_kernel(
 // the 32-bit scale words of the tile's key rows l, l+32, l+64, l+96 (rows past
 // the end of the key tensor get 0).  One thread per (tile, row).
 __global__ void __launch_bounds__(128) build_tiled_kscales_kernel(
-    const uint32_t* __restrict__ kscale_words, int64_t k_rows, const int32_t* __restrict__ cu_keys,
+    const uint8_t* __restrict__ kscale, int64_t k_rows, int replicate, const int32_t* __restrict__ cu_keys,
     const int* __restrict__ tile_base, int num_seqs, int max_tiles, uint32_t* __restrict__ out) {
   const int total = tile_base[num_seqs];
   const int r = threadIdx.x;
@@ -284,7 +285,11 @@ __global__ void __launch_bounds__(128) build_tiled_kscales_kernel(
       if (tile_base[mid] <= g) lo = mid; else hi = mid - 1;
     }
     const int64_t row = (int64_t)cu_keys[lo] + (int64_t)(g - tile_base[lo]) * kTileKeys + r;
-    out[(size_t)g * 128 + (r & 31) * 4 + (r >> 5)] = row < k_rows ? __ldg(kscale_words + row) : 0u;
+    uint32_t word = 0u;   // the row's four block scales (FP8: its one scale, four times)
+    if (row < k_rows)
+      word = replicate ? (uint32_t)__ldg(kscale + row) * 0x01010101u
+                       : __ldg(reinterpret_cast<const uint32_t*>(kscale) + row);
+    out[(size_t)g * 128 + (r & 31) * 4 + (r >> 5)] = word;
   }
 }
 
@@ -680,7 +685,7 @@ template <int PREC, int H>
 __global__ void __launch_bounds__(score_threads(PREC), 1)
     score_topk_kernel(const __grid_constant__ ScoreParams p) {
   constexpr bool MX = PREC == PREC_MXFP8;
-  constexpr bool F8 = PREC == PREC_FP8;                // one UE8M0 scale per row, folded in the epilogue
+  constexpr bool F8 = PREC == PREC_FP8;                // one UE8M0 scale per row (keys: in the MMA; q: in w)
   constexpr bool B1 = MX || F8;                        // one-byte operands
   constexpr int EW = epi_wgs(PREC);                   // epilogue warpgroups
   constexpr int QPW_MAX = qpw_max(PREC, H);           // queries per epilogue warpgroup
@@ -753,7 +758,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
       int it = 0;
       bool ok = true;
       const uint32_t q_bytes = pl.chunks * pl.qchunk + (MX ? pl.sfb_atoms * kSfRawWords * 4 : 0);
-      const uint32_t k_bytes = kStageBytes + (MX ? kSfTxBytes : 0);
+      const uint32_t k_bytes = kStageBytes + (B1 ? kSfTxBytes : 0);
       const int chunk_elems = kChunkBytes / (B1 ? 1 : 2);
       for (int r = 0; ok && r * G < nitems; ++r) {
         const int i = item_index(r, nitems);
@@ -787,7 +792,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
               mbar_arrive_expect_tx(bar_full(st), k_bytes);
               tma_load_2d(sbase + pl.k_off + st * kStageBytes, &p.tm_k, bar_full(st),
                           c * chunk_elems, krow);
-              if (MX)
+              if (B1)   // the tile's key scales, laid out for tcgen05.cp
                 bulk_load(sbase + pl.sfa_tx_off + st * kSfTxBytes,
                           p.ksf_tiles + (size_t)(m.ktile0 + t) * (kSfTxBytes / 4), kSfTxBytes,
                           bar_full(st));
@@ -825,13 +830,25 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
       uint32_t tcount = 0, st = 0, ph = 0;
       int it = 0;
       bool ok = true;
-      const uint32_t idesc = MX ? 0u : (F8 ? idesc_f8(128, pl.ncols) : idesc_bf16(128, pl.ncols));
+      const uint32_t idesc = B1 ? 0u : idesc_bf16(128, pl.ncols);
       uint32_t idesc_k[4];
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) idesc_k[kk] = idesc_mxf8(128, pl.ncols, kk);
       const uint64_t a_desc0 = sw128_kmajor_desc(sbase + pl.k_off, 0);    // stage 0, K step 0
       const uint64_t b_desc0 = sw128_kmajor_desc(sbase + pl.q_off, 0);    // chunk 0, K step 0
       const uint64_t sf_desc0 = sf_src_desc(sbase + pl.sfa_tx_off);       // stage 0 key scales
+      if (F8) {
+        // per-vector FP8 runs on the block-scaled MMA: the key rows' scales
+        // arrive per tile like MXFP8's (each replicated over the row's four
+        // blocks); the query rows' scales are folded into the head weights,
+        // so every query-scale atom holds 2^0 (0x7F), copied in once
+        uint32_t* unit = reinterpret_cast<uint32_t*>(smem + pl.sfb_tx_off);
+        for (int l = 0; l < kSfTxBytes / 4; ++l) unit[l] = 0x7F7F7F7Fu;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        for (int a = 0; a < pl.sfb_atoms; ++a)
+          tc_cp_32x128b_warpx4(tmem + kSfbCol + 4 * a, sf_src_desc(sbase + pl.sfb_tx_off));
+      }
       for (int r = 0; ok && r * G < nitems; ++r) {
         const int i = item_index(r, nitems);
         if (i < 0) continue;
@@ -875,15 +892,13 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             // descriptors: start address field + 2 per 32-byte K step
             const uint64_t ad0 = a_desc0 + (uint64_t)(st * (kStageBytes >> 4));
             const uint64_t bd0 = b_desc0 + (uint64_t)(c * (pl.qchunk >> 4));
-            if (MX)   // key scales arrive laid out for tcgen05.cp with the stage
+            if (B1)   // key scales arrive laid out for tcgen05.cp with the stage
               tc_cp_32x128b_warpx4(sfa, sf_desc0 + (uint64_t)(st * (kSfTxBytes >> 4)));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-              if (MX)
+              if (B1)
                 mma_mxf8(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc_k[kk], sfa, tmem + kSfbCol, acc);
-              else if (F8)
-                mma_f8(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
               else
                 mma_bf16(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
             }
@@ -979,12 +994,6 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
         for (int i = 0; i < 8; ++i) wp[i] = *reinterpret_cast<const float2*>(w_s + 8 * i + 2 * (lane & 3));
       }
       PT_ADD(5);
-      // FP8: UE8M0 byte of this thread's key row (local key index s), 127 past the end
-      auto key_scale_byte = [&](int s) -> int {
-        const int64_t krow = (int64_t)m.krow0 + s;
-        return krow < p.k_rows ? (int)__ldg(p.k_scale_vec + krow) : 127;
-      };
-      int kexp = F8 && m.ntiles > 0 ? key_scale_byte(orow) : 127;
       for (int tb = 0; tb < m.ntiles; tb += kBatch) {
         // ---- score kBatch tiles; keep keys and ballots in registers ----
         uint32_t bkey[kBatch][QPW_MAX];
@@ -1005,13 +1014,7 @@ __global__ void __launch_bounds__(score_threads(PREC), 1)
             TRACE(2 + v, tcount, tid == 0);   // warpgroup v woke on the tile's accumulator
             tc_fence_after();
             const int s_idx = t * kTileKeys + orow;     // local key (or pool) index of the reported row
-            // FP8: the key row's scale multiplies its score (sm_scale folded in);
-            // the next tile's scale byte is fetched now, a tile ahead of its use
-            float kfac = p.sm_scale;
-            if (F8) {
-              kfac = ldexpf(p.sm_scale, kexp - 127);
-              if (t + 1 < m.ntiles) kexp = key_scale_byte(s_idx + kTileKeys);
-            }
+            const float kfac = p.sm_scale;
             if constexpr (FRAG) {
               // Fragment layout (.16x256b): thread t holds 16 heads (2(t%4) + 8i, +1) of
               // the four key rows g, g+8, g+16, g+24 (g = t/4) of its warp's 32 rows, so
@@ -1381,13 +1384,13 @@ cudaError_t launch_build_worklist(const int32_t* cu, const int32_t* cu_k, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, const int32_t* cu_keys,
+cudaError_t launch_tiled_kscales(const uint8_t* k_scale, int64_t k_rows, int replicate, const int32_t* cu_keys,
                                  const int* tile_base, int num_seqs, int max_tiles, uint32_t* out,
                                  int sm_count, cudaStream_t stream) {
   int grid = max_tiles < sm_count * 8 ? max_tiles : sm_count * 8;
   if (grid < 1) grid = 1;
-  build_tiled_kscales_kernel<<<grid, 128, 0, stream>>>(reinterpret_cast<const uint32_t*>(k_scale), k_rows,
-                                                       cu_keys, tile_base, num_seqs, max_tiles, out);
+  build_tiled_kscales_kernel<<<grid, 128, 0, stream>>>(k_scale, k_rows, replicate, cu_keys, tile_base, num_seqs,
+                                                       max_tiles, out);
   return cudaGetLastError();
 }
 
