@@ -3,7 +3,8 @@
 // P consecutive keys becomes sum_i softmax_i(gate_i + bias_i) * k_i (softmax
 // over the P slots in FP32, BF16 gate, FP32 per-slot bias), stored as BF16.
 // Pooling restarts at document boundaries; a trailing incomplete group is not
-// pooled.  HBM-bound: one warp per pool, 128-bit loads.
+// pooled.  HBM-bound: one warp per pool, 128-bit loads (FP32 keys), the pool's
+// P rows requested together.
 #include <cuda_bf16.h>
 
 #include "dsa_device.cuh"
@@ -38,11 +39,41 @@ __global__ void __launch_bounds__(1024) kpool_cu_kernel(const int32_t* __restric
   if (tid == 0) cu_pools[num_seqs] = carry;
 }
 
+// Loads one key row slice (VEC values of lane `lane`) as FP32.
 template <int VEC>
+__device__ __forceinline__ void load_key(const void* k, int k_bf16, size_t row, float (&x)[VEC]) {
+  if (k_bf16) {
+    const uint16_t* kp = reinterpret_cast<const uint16_t*>(k) + row;
+    if constexpr (VEC == 4) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(kp));
+      x[0] = __uint_as_float(u.x << 16);
+      x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(u.y << 16);
+      x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(kp));
+      x[0] = __uint_as_float(u << 16);
+      x[1] = __uint_as_float(u & 0xFFFF0000u);
+    }
+  } else {
+    const float* kp = reinterpret_cast<const float*>(k) + row;
+    if constexpr (VEC == 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(kp));
+      x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    } else {
+      const float2 f = __ldg(reinterpret_cast<const float2*>(kp));
+      x[0] = f.x; x[1] = f.y;
+    }
+  }
+}
+
+// One warp per pool; the pool's P key rows are all requested before the gate
+// softmax is formed, so P loads per lane are in flight at once.
+template <int VEC, int P>
 __global__ void __launch_bounds__(256) kpool_compress_kernel(
     const void* __restrict__ k, int k_bf16, const uint16_t* __restrict__ gate,
     const float* __restrict__ bias, const int32_t* __restrict__ cu,
-    const int32_t* __restrict__ cu_pools, int num_seqs, int max_pools, int P,
+    const int32_t* __restrict__ cu_pools, int num_seqs, int max_pools,
     uint16_t* __restrict__ out) {
   constexpr int D = VEC * 32;
   const int lane = threadIdx.x & 31;
@@ -56,13 +87,18 @@ __global__ void __launch_bounds__(256) kpool_compress_kernel(
       if (cu_pools[mid] <= pi) lo = mid; else hi = mid - 1;
     }
     const int tok0 = cu[lo] + (pi - cu_pools[lo]) * P;
-    float logit[8];
+    float x[P][VEC];
+#pragma unroll
+    for (int i = 0; i < P; ++i) load_key<VEC>(k, k_bf16, (size_t)(tok0 + i) * D + lane * VEC, x[i]);
+    float logit[P];
     float mx = -INFINITY;
+#pragma unroll
     for (int i = 0; i < P; ++i) {
       logit[i] = __uint_as_float((uint32_t)__ldg(gate + tok0 + i) << 16) + __ldg(bias + i);
       mx = fmaxf(mx, logit[i]);
     }
     float den = 0.f;
+#pragma unroll
     for (int i = 0; i < P; ++i) {
       logit[i] = expf(logit[i] - mx);
       den += logit[i];
@@ -70,31 +106,33 @@ __global__ void __launch_bounds__(256) kpool_compress_kernel(
     float acc[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+#pragma unroll
     for (int i = 0; i < P; ++i) {
       const float wgt = logit[i] / den;
-      const size_t row = (size_t)(tok0 + i) * D + lane * VEC;
-      float x[VEC];
-      if (k_bf16) {
-        const uint16_t* kp = reinterpret_cast<const uint16_t*>(k) + row;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) x[e] = __uint_as_float((uint32_t)__ldg(kp + e) << 16);
-      } else {
-        const float* kp = reinterpret_cast<const float*>(k) + row;
-        if constexpr (VEC == 4) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(kp));
-          x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
-        } else {
-          const float2 f = __ldg(reinterpret_cast<const float2*>(kp));
-          x[0] = f.x; x[1] = f.y;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(wgt, x[e], acc[e]);
+      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(wgt, x[i][e], acc[e]);
     }
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)pi * D + lane * VEC;
 #pragma unroll
     for (int e = 0; e < VEC; e += 2) *reinterpret_cast<__nv_bfloat162*>(o + e) = __floats2bfloat162_rn(acc[e], acc[e + 1]);
   }
+}
+
+template <int VEC, int P>
+static void launch_kpool_p(const void* k, int k_bf16, const uint16_t* gate, const float* bias, const int32_t* cu,
+                           int num_seqs, int max_pools, uint16_t* out, const int32_t* cu_pools, int blocks,
+                           cudaStream_t stream) {
+  kpool_compress_kernel<VEC, P><<<blocks, 256, 0, stream>>>(k, k_bf16, gate, bias, cu, cu_pools, num_seqs,
+                                                            max_pools, out);
+}
+
+template <int VEC>
+static void launch_kpool_v(const void* k, int k_bf16, const uint16_t* gate, const float* bias, const int32_t* cu,
+                           int num_seqs, int max_pools, int P, uint16_t* out, const int32_t* cu_pools, int blocks,
+                           cudaStream_t stream) {
+  if (P == 2) launch_kpool_p<VEC, 2>(k, k_bf16, gate, bias, cu, num_seqs, max_pools, out, cu_pools, blocks, stream);
+  else if (P == 4) launch_kpool_p<VEC, 4>(k, k_bf16, gate, bias, cu, num_seqs, max_pools, out, cu_pools, blocks, stream);
+  else launch_kpool_p<VEC, 8>(k, k_bf16, gate, bias, cu, num_seqs, max_pools, out, cu_pools, blocks, stream);
 }
 
 cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const float* bias,
@@ -108,11 +146,9 @@ cudaError_t launch_kpool(const void* k, int k_bf16, const uint16_t* gate, const 
   int blocks = (max_pools + 7) / 8;
   if (blocks > sm_count * 8) blocks = sm_count * 8;
   if (D == 128)
-    kpool_compress_kernel<4><<<blocks, 256, 0, stream>>>(k, k_bf16, gate, bias, cu, cu_pools, num_seqs,
-                                                        max_pools, P, out);
+    launch_kpool_v<4>(k, k_bf16, gate, bias, cu, num_seqs, max_pools, P, out, cu_pools, blocks, stream);
   else
-    kpool_compress_kernel<2><<<blocks, 256, 0, stream>>>(k, k_bf16, gate, bias, cu, cu_pools, num_seqs,
-                                                        max_pools, P, out);
+    launch_kpool_v<2>(k, k_bf16, gate, bias, cu, num_seqs, max_pools, P, out, cu_pools, blocks, stream);
   return cudaGetLastError();
 }
 
