@@ -301,7 +301,7 @@ dsa_status_t dsa_idx_score_topk_kv(
  * GPU that loads the library holds until the process exits; sizes whose
  * dsa_idx_workspace_size exceeds 4 MiB are rejected with DSA_ERR_WORKSPACE
  * before anything is launched: about total_tokens + num_seqs above 524 000 for
- * BF16 and FP8 scoring, and total_tokens above about 349 000 for MXFP8 (its
+ * BF16 scoring, and total_tokens above about 349 000 for MXFP8 and FP8 (their
  * per-tile key scales also live in the scratch; each document costs about 43
  * tokens' worth more).  Comparing dsa_idx_workspace_size with 4194304 gives
  * the exact answer.  It calls no cudaMalloc/cudaFree.  The first call on each

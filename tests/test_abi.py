@@ -41,6 +41,13 @@ def test_host_only_functions(lib):
     ws = lib.dsa_idx_workspace_size(32768, 1, 32768, 64, 128, 2048, 1, _abi.DSA_PREC_MXFP8)
     assert ws >= 8 * 32768
     assert lib.dsa_idx_workspace_size(-1, 1, 0, 64, 128, 1, 1, 0) == 0
+    # the 8-bit formats keep one 512-byte key-scale tile per 128 keys (plus one
+    # per document) in the workspace; BF16 needs none
+    args = (32768, 3, 32768, 64, 128, 2048, 1)
+    bf = lib.dsa_idx_workspace_size(*args, _abi.DSA_PREC_BF16)
+    mx = lib.dsa_idx_workspace_size(*args, _abi.DSA_PREC_MXFP8)
+    f8 = lib.dsa_idx_workspace_size(*args, _abi.DSA_PREC_FP8)
+    assert mx == f8 == bf + 512 * (32768 // 128 + 3 + 1)
 
 
 def test_host_argument_checks_precede_any_cuda_call(lib):
