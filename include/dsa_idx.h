@@ -336,16 +336,8 @@ dsa_status_t dsa_idx_score_topk_noalloc_status(dsa_stream_t stream, dsa_status_t
 dsa_status_t dsa_idx_read_status(const void* ws, dsa_stream_t stream,
                                  dsa_status_t* out);
 
-/* Diagnostic: one tcgen05 tile of the scoring contraction, written raw.
- * acc[r, c] = sum_d K[r, d] * Q[c, d] for r < 128 key rows starting at
- * k_row0 and c < n_cols query rows starting at q_row0 (block-scaled for
- * MXFP8), fp32 [128, n_cols] to `acc_out`.  Used by the tests to check the
- * tensor-core operand layout in isolation; not on the hot path. */
-dsa_status_t dsa_idx_debug_mma_tile(
-    const void* q, const uint8_t* q_scale, int64_t q_rows, int64_t q_row0,
-    const void* k, const uint8_t* k_scale, int64_t k_rows, int64_t k_row0,
-    int head_dim, int n_cols, dsa_precision_t prec, float* acc_out,
-    void* ws, size_t ws_bytes, dsa_stream_t stream);
+/* Test-only entry points (a raw tensor-core tile, the timeout and the
+ * fault-injection hooks) are declared in dsa_idx_testing.h. */
 
 #ifdef __cplusplus
 }

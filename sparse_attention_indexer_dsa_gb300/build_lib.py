@@ -39,7 +39,7 @@ def _sources():
 
 def _headers():
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    hs.append(os.path.join(ROOT, "include", "dsa_idx.h"))
+    hs += [os.path.join(ROOT, "include", h) for h in ("dsa_idx.h", "dsa_idx_testing.h")]
     return hs
 
 

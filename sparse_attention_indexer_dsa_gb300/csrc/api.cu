@@ -13,6 +13,7 @@
 #include <string>
 
 #include "dsa_idx.h"
+#include "dsa_idx_testing.h"
 #include "dsa_status_codes.h"
 #include "dsa_params.h"
 
@@ -513,9 +514,9 @@ dsa_status_t dsa_idx_debug_mma_tile(const void* q, const uint8_t* q_scale, int64
   return DSA_OK;
 }
 
-// Test hooks (not part of the public header): the bounded-wait limit of the
-// fused kernel, and a fault injection that withholds its first key stage so
-// the timeout path runs without faulting the GPU.
+// Test hooks (dsa_idx_testing.h): the bounded-wait limit of the fused kernel,
+// and a fault injection that withholds its first key stage so the timeout
+// path runs without faulting the GPU.
 void dsa_idx_test_set_timeout_ns(unsigned long long ns) { g_timeout_ns = ns; }
 void dsa_idx_test_set_fault_inject(int mode) { g_fault_inject = mode; }
 

@@ -19,7 +19,7 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "dsa_idx.h")).read()
+    src = "".join(open(os.path.join(ROOT, "include", h)).read() for h in ("dsa_idx.h", "dsa_idx_testing.h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(dsa_idx_\w+)\s*\(", src)))
 
