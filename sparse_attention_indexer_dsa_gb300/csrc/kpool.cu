@@ -68,9 +68,12 @@ __device__ __forceinline__ void load_key(const void* k, int k_bf16, size_t row, 
 }
 
 // One warp per pool; the pool's P key rows are all requested before the gate
-// softmax is formed, so P loads per lane are in flight at once.
+// softmax is formed, so P loads per lane are in flight at once.  Eight
+// resident blocks per SM (32 registers) for P <= 4 keep enough bytes in
+// flight (measured 79 % of the copy bandwidth against 74 % at four); P = 8
+// holds twice the rows and stays at four.
 template <int VEC, int P>
-__global__ void __launch_bounds__(256) kpool_compress_kernel(
+__global__ void __launch_bounds__(256, P <= 4 ? 8 : 4) kpool_compress_kernel(
     const void* __restrict__ k, int k_bf16, const uint16_t* __restrict__ gate,
     const float* __restrict__ bias, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ cu_pools, int num_seqs, int max_pools,
