@@ -461,7 +461,7 @@ def run_native(args, wl):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.5)    # nvidia-smi's start-up holds the driver for a moment: keep it out of the timed loop
+    time.sleep(0.5)    # nvidia-smi's start-up holds the NVIDIA kernel driver for a moment: keep it out of the timed loop
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                      # L2 flush, outside the events

@@ -1,5 +1,5 @@
-"""Two-rank paths of bench.py on CPU (gloo), launched as the driver launches
-them: torchrun, one process per rank, rendezvous on 127.0.0.1."""
+"""Two-rank paths of bench.py on CPU (gloo), launched the way a multi-GPU
+bench run is: torchrun, one process per rank, rendezvous on 127.0.0.1."""
 import json
 import os
 import socket
