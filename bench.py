@@ -234,8 +234,8 @@ def run_table(args):
     cases = [("tiny", "bf16"), ("c2", "bf16"), ("c3", "mxfp8"), ("c3", "bf16"), ("thd", "mxfp8"),
              ("kpool", "bf16"), ("target", "mxfp8"), ("target", "bf16"), ("target", "fp8")]
     print(f"| config | precision | score+top-k ms | queries/s | TFLOP/s | % of {peak_kind} peak | "
-          f"oracle queries/s ({os.cpu_count()} cores, rows) |")
-    print("|---|---|---:|---:|---:|---:|---:|")
+          f"top-k overlap with BF16 (mean / min) | oracle queries/s ({os.cpu_count()} cores, rows) |")
+    print("|---|---|---:|---:|---:|---:|---:|---:|")
     fp8_peak, _ = measure_fp8_peak(devn)
     for name, prec in cases:
         wl = W.config(name)
@@ -274,14 +274,40 @@ def run_table(args):
         if dsa.read_status(ws) != 0:
             raise RuntimeError(f"{name} {prec}: device status {dsa.read_status(ws)}")
         ms = statistics.median(ts)
+        overlap = "—"
+        if prec != "bf16":   # the same inputs scored in BF16: how many of the 8-bit picks agree
+            ia, _, la = run()
+            qb, _, kb, _ = dsa.preprocess(q, k, cu, wl.max_seqlen, g, b, 1e-6, wl.rope_dim, wl.rope_base, False,
+                                          True, "bf16")
+            wsb = dsa.workspace(T, len(wl.doc_lens), wl.max_seqlen, H, D, K, wl.kpool, "bf16", devn)
+            ib, _, lb = dsa.score_topk(qb, None, kb, None, w, cu, wl.max_seqlen, H, K, "bf16", ws=wsb, **pool)
+            mean, mn = topk_overlap(ia, la, ib, lb)
+            overlap = f"{mean:.4f} / {mn:.4f}"
+            del qb, kb, wsb, ib, lb
         tf = wl.flops() / ms / 1e9
         peak = fp8_peak if prec in ("mxfp8", "fp8") else peaks["bf16_tflops"]
         n_rows = min(T, args.ref_rows // 8 if T > 4096 else 64)
         orate, _ = oracle_rate(wl, x, prec, n_rows)
         print(f"| {describe(wl, prec)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
-              f"{100 * tf / peak:.1f} | {orate:,.1f} ({n_rows}) |", flush=True)
+              f"{100 * tf / peak:.1f} | {overlap} | {orate:,.1f} ({n_rows}) |", flush=True)
     print(f"\nPeaks: BF16 {peaks['bf16_tflops']:.1f} TFLOP/s ({peak_kind}); FP8 {fp8_peak:.1f} TFLOP/s "
           f"(E4M3 GEMM measured in this run) for the MXFP8 and FP8 rows.", flush=True)
+
+
+def topk_overlap(idx_a, len_a, idx_b, len_b):
+    """Per-row overlap |A & B| / max(|A|, 1) of two top-k outputs in index
+    order (device tensors [T, W] and lengths [T]); returns (mean, min).  Rows
+    are ascending, so each entry of A is looked up in B by binary search."""
+    import torch
+    big = torch.iinfo(torch.int32).max
+    w = idx_a.shape[1]
+    col = torch.arange(w, device=idx_a.device)[None, :]
+    a = torch.where(col < len_a[:, None], idx_a, big)
+    b = torch.where(col < len_b[:, None], idx_b, big).contiguous()
+    pos = torch.searchsorted(b, a.contiguous()).clamp(max=w - 1)
+    hit = (torch.gather(b, 1, pos) == a) & (a != big)
+    ov = hit.sum(1).double() / len_a.clamp(min=1).double()
+    return float(ov.mean()), float(ov.min())
 
 
 def _median_ms(fn, flush, stream, reps=5, warm=2):
