@@ -23,7 +23,7 @@ class Workload:
     n_heads: int
     head_dim: int
     index_topk: int
-    prec: str                 # "bf16" or "mxfp8"
+    prec: str                 # "bf16", "mxfp8" or "fp8" (one scale per vector)
     values: str               # "int" | "normal" | "outlier"
     layernorm: bool = False
     rope_dim: int = 0

@@ -75,12 +75,16 @@ def _operands(prec, T, H, D, seed):
     if prec == "bf16":
         qb, kb = O.float_to_bf16_bits(O.round_bf16(q)), O.float_to_bf16_bits(O.round_bf16(k))
         return [bf16_dev(qb), None, bf16_dev(kb), None], _abi.DSA_PREC_BF16
+    if prec == "fp8":
+        qc, qs, _ = O.quantize_fp8_rows(q)
+        kc, ks, _ = O.quantize_fp8_rows(k)
+        return [dev(qc), dev(qs), dev(kc), dev(ks)], _abi.DSA_PREC_FP8
     qc, qs, _ = O.quantize_mxfp8(q)
     kc, ks, _ = O.quantize_mxfp8(k)
     return [dev(qc), dev(qs), dev(kc), dev(ks)], _abi.DSA_PREC_MXFP8
 
 
-@pytest.mark.parametrize("prec", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("prec", ["bf16", "mxfp8", "fp8"])
 @pytest.mark.parametrize("order", ["index", "score"])
 def test_checked_build_matches_and_stays_in_bounds(chk, prec, order):
     lens, H, D, k = [300, 5, 700], 64, 128, 64

@@ -81,3 +81,26 @@ def test_kpool_mxfp8_scoring():
     ref = O.kpool_topk(qq.reshape(T, H, D), kq, x["w"].astype(np.float64), wl.cu_seqlens, rcp, wl.index_topk, P,
                        True, rows=rows, with_scale=True)
     compare_topk(host(idx), host(sc), host(ln), ref, REL_MXFP8, pool=P, tail=True, rows=rows)
+
+
+def test_kpool_fp8_scoring():
+    """KPool with per-vector FP8 scoring: the pooled BF16 keys get one UE8M0
+    scale per pooled row (dsa_idx_quantize_fp8_rows), laid out per key tile
+    for the block-scaled MMA like the MXFP8 key scales.  Same reasoning and
+    tolerance as the MXFP8 case."""
+    wl = W.Workload("kpool-f8", [2600, 700], 64, 128, 2048, "fp8", "normal", w_std=0.125, kpool=4, seed=1011)
+    x = W.make_inputs(wl)
+    T, H, D, P = wl.total_tokens, wl.n_heads, wl.head_dim, wl.kpool
+    cu = dev(wl.cu_seqlens)
+    kp, cp = dsa.kpool_compress(dev(x["k"]), dev(x["gate_bits"].view(np.int16)), dev(x["slot_bias"]), cu, P)
+    kc, ks = dsa.quantize_fp8_rows(kp)
+    qc, qs = dsa.quantize_fp8_rows(dev(x["q"].reshape(T * H, D)))
+    idx, sc, ln = dsa.score_topk(qc, qs, kc, ks, dev(x["w"]), cu, wl.max_seqlen, H, wl.index_topk, "fp8",
+                                 kpool_size=P, cu_pools=cp, tail=True)
+    kbar, rcp = O.kpool_compress(x["k"], O.bf16_bits_to_float(x["gate_bits"]), x["slot_bias"], wl.cu_seqlens, P)
+    _, _, kq = O.quantize_fp8_rows(O.round_bf16(kbar))
+    _, _, qq = O.quantize_fp8_rows(x["q"].reshape(T * H, D).astype(np.float64))
+    rows = np.concatenate([np.arange(0, 40), np.arange(2560, 2620), np.arange(T - 40, T)])
+    ref = O.kpool_topk(qq.reshape(T, H, D), kq, x["w"].astype(np.float64), wl.cu_seqlens, rcp, wl.index_topk, P,
+                       True, rows=rows, with_scale=True)
+    compare_topk(host(idx), host(sc), host(ln), ref, REL_MXFP8, pool=P, tail=True, rows=rows)

@@ -62,13 +62,13 @@ def _twice(lib, ops, w, cu, lens, H, D, k, p, W_, ref, **kw):
             assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("prec", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("prec", ["bf16", "mxfp8", "fp8"])
 @pytest.mark.parametrize("order", ["index", "score"])
 def test_noalloc_matches_workspace_entry_point_twice(prec, order):
     lib = _abi.load()
     lens, H, D, k = [700, 1, 260], 64, 128, 96
     cu, _, w, ops = _inputs(prec, lens, H, D)
-    p = dsa.DSA_PREC_BF16 if prec == "bf16" else dsa.DSA_PREC_MXFP8
+    p = {"bf16": dsa.DSA_PREC_BF16, "mxfp8": dsa.DSA_PREC_MXFP8, "fp8": dsa.DSA_PREC_FP8}[prec]
     ref = dsa.score_topk(*ops, w, cu, max(lens), H, k, prec, sm_scale=0.5, order=order)
     flags = _abi.DSA_FLAG_DETERMINISTIC | (_abi.DSA_FLAG_SORT_BY_SCORE if order == "score" else 0)
     _twice(lib, ops, w, cu, lens, H, D, k, p, k, ref, flags=flags)
