@@ -290,8 +290,85 @@ def run_table(args):
         orate, _ = oracle_rate(wl, x, prec, n_rows)
         print(f"| {describe(wl, prec)} | {prec.upper()} | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | "
               f"{100 * tf / peak:.1f} | {overlap} | {orate:,.1f} ({n_rows}) |", flush=True)
+    table_extra_rows(dsa, devn, flush, fp8_peak)
     print(f"\nPeaks: BF16 {peaks['bf16_tflops']:.1f} TFLOP/s ({peak_kind}); FP8 {fp8_peak:.1f} TFLOP/s "
           f"(E4M3 GEMM measured in this run) for the MXFP8 and FP8 rows.", flush=True)
+
+
+def table_extra_rows(dsa, devn, flush, fp8_peak):
+    """Rows for the paths beyond the plain causal one, MXFP8 throughout, timed
+    like the table's other rows (no oracle column):
+      * KPool (P = 4) with MXFP8 scoring of the pooled keys;
+      * caller-provided compressed keys, ratio 4, top-2048 compressed keys;
+      * queries that are the last 8192 of 32768 key tokens (global causal
+        offsets), top-2048.
+    TFLOP/s from the algorithmic 2*H*D per visible (query, key) pair."""
+    import torch
+    H, D, K = 64, 128, 2048
+
+    def timed(run):
+        for _ in range(2):
+            run()
+        ts = []
+        for r in range(5):
+            flush.fill_(r)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def row(label, T, ms, pairs):
+        tf = 2.0 * H * D * pairs / ms / 1e9
+        print(f"| {label} | MXFP8 | {ms:.3f} | {T / ms * 1e3:,.0f} | {tf:.1f} | {100 * tf / fp8_peak:.1f} | — | — |",
+              flush=True)
+
+    # KPool with MXFP8 scoring: pooled BF16 keys quantised like every other operand
+    wl = W.config("kpool")
+    x = W.make_inputs(wl)
+    T, P = wl.total_tokens, wl.kpool
+    cu = torch.from_numpy(wl.cu_seqlens).to(devn)
+    qc, qs = dsa.quantize_mxfp8(torch.from_numpy(x["q"].reshape(T * H, D)).to(devn))
+    kp, cp = dsa.kpool_compress(torch.from_numpy(x["k"]).to(devn),
+                                torch.from_numpy(x["gate_bits"].view(np.int16)).to(devn),
+                                torch.from_numpy(x["slot_bias"]).to(devn), cu, P)
+    kc, ks = dsa.quantize_mxfp8(kp)
+    w = torch.from_numpy(x["w"]).to(devn)
+    ws = dsa.workspace(T, 1, wl.max_seqlen, H, D, wl.index_topk, P, "mxfp8", devn)
+    ms = timed(lambda: dsa.score_topk(qc, qs, kc, ks, w, cu, wl.max_seqlen, H, wl.index_topk, "mxfp8", ws=ws,
+                                      kpool_size=P, cu_pools=cp, tail=True))
+    row(f"kpool: 1×{T}, P = {P}, top-{wl.index_topk // P} pools + tail, pooled keys in MXFP8", T, ms,
+        wl.causal_pairs())
+    del qc, qs, kp, kc, ks, ws
+
+    # compressed keys, ratio 4: query t sees floor((t+1)/4) compressed keys
+    T, r = 32768, 4
+    rng = np.random.default_rng(2024)
+    qc, qs = dsa.quantize_mxfp8(torch.from_numpy(rng.standard_normal((T * H, D), dtype=np.float32)).to(devn))
+    kc, ks = dsa.quantize_mxfp8(torch.from_numpy(rng.standard_normal((T // r, D), dtype=np.float32)).to(devn))
+    w = torch.from_numpy((rng.standard_normal((T, H)) * 0.125).astype(np.float32)).to(devn)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=devn)
+    cc = torch.tensor([0, T // r], dtype=torch.int32, device=devn)
+    ws = dsa.workspace(T, 1, T, H, D, K, r, "mxfp8", devn)
+    ms = timed(lambda: dsa.score_topk(qc, qs, kc, ks, w, cu, T, H, K, "mxfp8", ws=ws, kpool_size=r, cu_pools=cc,
+                                      compressed=True))
+    row(f"compressed keys: 1×{T} queries, ratio {r} ({T // r} keys), top-{K}", T, ms,
+        sum((t + 1) // r for t in range(T)))
+    del qc, qs, kc, ks, ws
+
+    # global causal offsets: the last Tq of S key tokens
+    S, Tq = 32768, 8192
+    qc, qs = dsa.quantize_mxfp8(torch.from_numpy(rng.standard_normal((Tq * H, D), dtype=np.float32)).to(devn))
+    kc, ks = dsa.quantize_mxfp8(torch.from_numpy(rng.standard_normal((S, D), dtype=np.float32)).to(devn))
+    w = torch.from_numpy((rng.standard_normal((Tq, H)) * 0.125).astype(np.float32)).to(devn)
+    cq = torch.tensor([0, Tq], dtype=torch.int32, device=devn)
+    ck = torch.tensor([0, S], dtype=torch.int32, device=devn)
+    ws = dsa.workspace(S, 1, S, H, D, K, 1, "mxfp8", devn)
+    ms = timed(lambda: dsa.score_topk_kv(qc, qs, kc, ks, w, cq, ck, Tq, S, H, K, "mxfp8", ws=ws))
+    row(f"key offsets: the last {Tq} of {S} tokens as queries, top-{K}", Tq, ms,
+        sum(S - Tq + i + 1 for i in range(Tq)))
 
 
 def topk_overlap(idx_a, len_a, idx_b, len_b):
