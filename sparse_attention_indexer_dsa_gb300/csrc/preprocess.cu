@@ -1,21 +1,27 @@
 // Query/key preprocessing and MXFP8 / per-vector FP8 quantisation for sm_103a
 // (HBM-bound).
 //
-// * preprocess_kernel: key LayerNorm -> RoPE -> BF16 or MXFP8, one block per
-//   token (its H query rows + its key row), one warp per row, 128-bit loads,
-//   warp-shuffle reductions.  Megatron-LM PR #8403 "cuDNN DSA indexer
+// * preprocess_kernel: key LayerNorm -> RoPE -> BF16, MXFP8 or per-vector
+//   FP8, one block per token (its H query rows + its key row), one warp per
+//   row, 128-bit loads, warp-shuffle reductions; the output format, RoPE
+//   layout and BF16 mid-rounding are template parameters, so a row's code has
+//   no branches.  Megatron-LM PR #8403 "cuDNN DSA indexer
 //   precision options": "What does this PR do?" (dsa_indexer_rope_fp32 keeps
 //   the key LayerNorm -> RoPE chain in FP32) and "Motivation" (the default
 //   path materialises BF16 between the LayerNorm and RoPE); review finding 2
 //   (BF16 scoring rounds FP32 carriers to BF16).  PR #7522 "Changes": NoPE
 //   (rope_dim = 0).  PR #5992 "Key changes": MXFP8 scoring operands.
 // * quantize_mxfp8_kernel: stand-alone FP32/BF16 -> E4M3 + UE8M0 per 32
-//   elements (PR #5992 "Key changes", BF16 -> MXFP8 quantisation).
+//   elements (PR #5992 "Key changes", BF16 -> MXFP8 quantisation);
+//   quantize_fp8_rows_kernel: the same with one UE8M0 scale per 128-element
+//   row (PR #8403 "What does this PR do?", the per-vector FP8 path).
 //
 // MXFP8 block rule (DSA_MX_SCALE_NOSAT): the UE8M0 exponent is the smallest e
 // with amax <= 448 * 2^e, found from the exponent and mantissa bits of amax
-// (448 = 1.75 * 2^8); the payload is RNE(x * 2^-e) to E4M3 with saturation
-// (hardware cvt.rn.satfinite).  DSA_MX_SCALE_FLOOR: e = floor(log2 amax) - 8.
+// (448 = 1.75 * 2^8, see mx_exponent_bits); the payload is RNE(x * 2^-e) to
+// E4M3 with saturation (hardware cvt.rn.satfinite).  DSA_MX_SCALE_FLOOR:
+// e = floor(log2 amax) - 8.  Non-finite inputs give unspecified codes (the
+// checked build's input scan covers the scoring call, not these kernels).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
