@@ -150,7 +150,9 @@ int dsa_idx_output_width(int index_topk, int kpool_size, int flags);
  *   q_scale_out device u8 [total_tokens*n_heads, head_dim/32] (MXFP8) or
  *           [total_tokens*n_heads] (FP8), else NULL
  *   k_out, k_scale_out  same for the keys ([total_tokens, ...])
- * Supported: head_dim in {64,128} (MXFP8 and FP8: 128), n_heads in {1..64}. */
+ * Supported: head_dim in {64,128} (MXFP8 and FP8: 128), n_heads in {1..64}.
+ * Non-finite inputs give unspecified outputs (no status is recorded: the
+ * checked build scans the scoring call's operands instead). */
 dsa_status_t dsa_idx_preprocess(
     const void* q, const void* k, dsa_dtype_t in_dtype,
     const float* ln_gamma, const float* ln_beta, float ln_eps,
@@ -166,25 +168,27 @@ dsa_status_t dsa_idx_preprocess(
  *   x        device [rows, cols] in_dtype
  *   x_e4m3   device u8 [rows, cols]
  *   x_ue8m0  device u8 [rows, cols/32]
- * cols must be a multiple of 32 (64 or 128 for the scoring kernel). */
+ * cols must be a multiple of 32 (64 or 128 for the scoring kernel).
+ * Non-finite elements give unspecified codes (as in dsa_idx_preprocess). */
+dsa_status_t dsa_idx_quantize_mxfp8(const void* x, dsa_dtype_t in_dtype,
+                                    int64_t rows, int cols,
+                                    dsa_mx_scale_rule_t scale_rule,
+                                    uint8_t* x_e4m3, uint8_t* x_ue8m0,
+                                    dsa_stream_t stream);
+
 /* Stand-alone BF16/FP32 -> FP8 with one UE8M0 scale per row (the per-vector
  * FP8 scoring of [P1] "What does this PR do?"); the row exponent follows the
  * same rule as an MXFP8 block (scale_rule).
  *   x        device [rows, 128] in_dtype, 16-byte aligned
  *   x_e4m3   device u8 [rows, 128]
  *   x_ue8m0  device u8 [rows]
- * cols must be 128 (DSA_ERR_UNSUPPORTED otherwise). */
+ * cols must be 128 (DSA_ERR_UNSUPPORTED otherwise).  Non-finite elements give
+ * unspecified codes. */
 dsa_status_t dsa_idx_quantize_fp8_rows(const void* x, dsa_dtype_t in_dtype,
                                        int64_t rows, int cols,
                                        dsa_mx_scale_rule_t scale_rule,
                                        uint8_t* x_e4m3, uint8_t* x_ue8m0,
                                        dsa_stream_t stream);
-
-dsa_status_t dsa_idx_quantize_mxfp8(const void* x, dsa_dtype_t in_dtype,
-                                    int64_t rows, int cols,
-                                    dsa_mx_scale_rule_t scale_rule,
-                                    uint8_t* x_e4m3, uint8_t* x_ue8m0,
-                                    dsa_stream_t stream);
 
 /* KPool key compression ([P3] "Changes", dsa_indexer_kpool > 1): in every
  * document, each complete group of pool_size consecutive keys becomes
