@@ -70,3 +70,24 @@ def test_reference_arm_line_keeps_the_contract():
     assert set(d["cpu_baseline"]) >= {"value", "unit", "cores", "kind", "sample"}
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert abs(d["ms_per_step"] * d["steps"] / 1e3 * d["value"] - 2 * 8) < 1e-6 * d["value"] + 1e-6
+
+
+def test_topk_overlap_helper():
+    """bench.py's per-row top-k overlap (used by the table's MXFP8-vs-BF16
+    column): ascending rows with -1 padding past each row's length."""
+    import importlib.util
+
+    import torch
+
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    a = torch.tensor([[1, 3, 5, -1], [2, 4, 6, 8], [7, -1, -1, -1]], dtype=torch.int32)
+    b = torch.tensor([[1, 5, 7, -1], [2, 4, 6, 8], [0, 9, -1, -1]], dtype=torch.int32)
+    la = torch.tensor([3, 4, 1])
+    lb = torch.tensor([3, 4, 2])
+    mean, mn = bench.topk_overlap(a, la, b, lb)
+    assert abs(mean - (2 / 3 + 1 + 0) / 3) < 1e-12 and mn == 0.0
+    # a row against itself overlaps fully, padding never counts
+    mean, mn = bench.topk_overlap(a, la, a, la)
+    assert mean == 1.0 and mn == 1.0
