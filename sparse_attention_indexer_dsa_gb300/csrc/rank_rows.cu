@@ -8,7 +8,7 @@
 // mode the unit is a pool (its P consecutive tokens share one score and move
 // together), so rows of up to 4096 pools rank at pool granularity.
 //
-// Bucket rank (the common case): every unit is put in one of 2U buckets by a
+// Bucket rank (the common case): every unit is put in one of U buckets by a
 // monotone map of its score, so a unit's final position is the number of
 // units in higher buckets plus the number of units of its own bucket that
 // rank before it (higher score, or equal score and lower index), counted by
@@ -19,7 +19,12 @@
 // rounded float add, an integer difference or a multiply by a positive
 // constant, each monotone, so the map never reorders two scores.  One pass
 // over shared memory: count (shared atomics give each unit a slot in its
-// bucket), scan, scatter, count the members ahead, place.
+// bucket), scan, scatter into bucket order, then place: each thread takes
+// staged positions, so the lanes of a warp hold neighbouring buckets (their
+// member loads broadcast and their loop counts agree), counts the members of
+// the position's bucket that rank before it, and writes the unit to its final
+// place (single entries straight into the output row, whose writes then fall
+// on neighbouring addresses).
 //
 // Radix rank (the fallback, for rows whose largest bucket holds more than
 // kBucketCap units: many tied scores, or a distribution the map does not
@@ -46,10 +51,7 @@ constexpr int kRankThreads = 256;
 constexpr int kRankWarps = kRankThreads / 32;
 constexpr int kDigits = 16;           // 4-bit digits of the radix fallback
 constexpr int kBucketCap = 64;        // larger bucket: the row takes the radix fallback
-#ifndef RANK_NB_MUL
-#define RANK_NB_MUL 2
-#endif
-constexpr int kBucketsPerUnit = RANK_NB_MUL;   // buckets per rankable unit
+constexpr int kBucketsPerUnit = 1;   // buckets per rankable unit
 
 __device__ __forceinline__ int padded(int g) { return g + (g >> 5); }
 
@@ -82,8 +84,9 @@ template <int U>
 struct BucketSmem {
   static constexpr int kBuckets = U * kBucketsPerUnit;
   uint64_t stage[U];   // units grouped by bucket: key << 32 | ~index (larger ranks first)
-  uint64_t fin[U];     // units in ranking order
+  uint64_t fin[U];     // units in ranking order (KPool pools; single entries go straight to the row)
   uint32_t cnt[kBuckets + kBuckets / 32];   // bucket counters, then start | count << 13 (padded)
+  uint16_t bkt[U];     // bucket of each staged unit
 };
 
 template <int U>
@@ -251,48 +254,41 @@ __device__ __forceinline__ bool bucket_rank(RankSmem<kRankThreads * E>& sm, uint
     sm.b.cnt[padded(tid * EB + i)] = ((uint32_t)n - before) | (cv << 13);
   }
   __syncthreads();
-  // scatter into the buckets; bs becomes start | count << 13 | slot << 20
-  // (count <= kBucketCap < 2^7, slot < count)
+  // scatter into bucket order (count <= kBucketCap < 2^7, start < 2^13)
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int u = e * kRankThreads + tid;
     if (FULL || u < n) {
       const uint32_t bv = sm.b.cnt[padded((int)(bs[e] & 0xFFFFu))];
       const uint32_t slot = bs[e] >> 16;
-      sm.b.stage[(bv & 0x1FFFu) + slot] =
-          ((uint64_t)score_key(ls[e]) << 32) | (uint32_t)~(uint32_t)li[e];
-      bs[e] = bv | (slot << 20);
+      const uint32_t at = (bv & 0x1FFFu) + slot;
+      sm.b.stage[at] = ((uint64_t)score_key(ls[e]) << 32) | (uint32_t)~(uint32_t)li[e];
+      sm.b.bkt[at] = (uint16_t)(bs[e] & 0xFFFFu);
     }
   }
   __syncthreads();
-  // final position: the bucket's start plus the members that rank before this unit
+  // final position: the bucket's start plus the members that rank before the
+  // unit, taken over staged positions (a warp's lanes hold neighbouring buckets)
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int u = e * kRankThreads + tid;
-    if (FULL || u < n) {
-      const uint64_t pk = ((uint64_t)score_key(ls[e]) << 32) | (uint32_t)~(uint32_t)li[e];
-      const uint32_t st = bs[e] & 0x1FFFu, m = (bs[e] >> 13) & 0x7Fu;
+    const int p = e * kRankThreads + tid;
+    if (FULL || p < n) {
+      const uint64_t pk = sm.b.stage[p];
+      const uint32_t bv = sm.b.cnt[padded((int)sm.b.bkt[p])];
+      const uint32_t st = bv & 0x1FFFu, m = (bv >> 13) & 0x7Fu;
       uint32_t pos = st;
-      if (m == 2u) {
-        pos += sm.b.stage[st + ((bs[e] >> 20) ^ 1u)] > pk ? 1u : 0u;
-      } else if (m > 2u) {
+      if (m > 1u)
         for (uint32_t j = 0; j < m; ++j) pos += sm.b.stage[st + j] > pk ? 1u : 0u;
+      if (SINGLE) {   // the row's loads were all taken before the first barrier
+        ri[pos] = (int32_t)~(uint32_t)pk;
+        rs[pos] = key_score((uint32_t)(pk >> 32));
+      } else {
+        sm.b.fin[pos] = pk;
       }
-      sm.b.fin[pos] = pk;
     }
   }
-  __syncthreads();
-  if (SINGLE) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int g = e * kRankThreads + tid;
-      if (FULL || g < n) {
-        const uint64_t v = sm.b.fin[g];
-        ri[g] = (int32_t)~(uint32_t)v;
-        rs[g] = key_score((uint32_t)(v >> 32));
-      }
-    }
-  } else {
+  __syncthreads();   // every read of the counters and the stage before they are reused
+  if (!SINGLE) {
     for (int g = tid; g < n * group; g += kRankThreads) {
       const int u = g / group;
       const uint64_t v = sm.b.fin[u];

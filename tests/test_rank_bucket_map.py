@@ -14,7 +14,9 @@ mul = floor(float(NB * 2^32 * (1 - 2^-20)) / float_ru(range + 1)).
 import numpy as np
 import pytest
 
-NB = 4096   # buckets of a 2048-unit row (two per unit)
+# bucket counts of the kernel's row sizes (one bucket per rankable unit slot:
+# 256, 2048 and 4096 units), and twice the largest
+NBS = (256, 2048, 4096, 8192)
 
 
 def _bits(x):
@@ -34,7 +36,7 @@ def _round_up(x):
     return np.nextafter(f, np.float32(np.inf)) if float(f) < x else f
 
 
-def _buckets(v):
+def _buckets(v, NB):
     v = np.asarray(v, np.float32)
     vmin, vmax = v.min(), v.max()
     with np.errstate(over="ignore", invalid="ignore"):
@@ -44,7 +46,7 @@ def _buckets(v):
     x = (_coord(v, c) + np.uint64((1 << 32) - lo)) & np.uint64(0xFFFFFFFF)
     if rng < NB:
         return x.astype(np.int64)
-    num = np.float32(NB * 4294967296.0 * (1.0 - 2.0 ** -20))   # exact: 2^44 - 2^24
+    num = np.float32(NB * 4294967296.0 * (1.0 - 2.0 ** -20))   # exact: NB * (2^32 - 2^12)
     den = _round_up(float(_round_up(rng)) + 1.0)
     mul = int(np.floor(np.float64(np.float32(np.float64(num) / np.float64(den)))))
     assert 0 < mul < 2 ** 32
@@ -61,8 +63,9 @@ def _dists(rng, n):
     yield np.where(rng.random(n) < 0.01, 2.0 ** 20, 1.0) * np.abs(rng.standard_normal(n))
 
 
+@pytest.mark.parametrize("NB", NBS)
 @pytest.mark.parametrize("seed", range(6))
-def test_bucket_map_is_monotone_and_in_range(seed):
+def test_bucket_map_is_monotone_and_in_range(seed, NB):
     rng = np.random.default_rng(seed)
     for n in (2, 37, 2048):
         for v in _dists(rng, n):
@@ -71,7 +74,7 @@ def test_bucket_map_is_monotone_and_in_range(seed):
             v = v[np.isfinite(v)]
             if v.size < 2 or v.min() == v.max():
                 continue
-            b = _buckets(v)
+            b = _buckets(v, NB)
             assert b.min() >= 0 and b.max() < NB
             order = np.argsort(v, kind="stable")
             assert np.all(np.diff(b[order]) >= 0), "a larger score landed in a lower bucket"
